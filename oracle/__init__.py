@@ -1,0 +1,181 @@
+"""CPU oracle of the FP8 (E4M3) fine-grained-scaled GEMM — TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg (and its
+``--impl reference`` arm) may import this package. The CUDA path never does; the two share no
+code. ``dg_oracle.cpp`` holds the arithmetic and documents, function by function, which passage
+of the DeepGEMM pages (or which outside definition: OCP E4M3, IEEE rounding, the DeepSeek-V3
+scale granularity) it follows.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against things other than itself:
+the OCP E4M3 table and torch's float8 conversion, torch's float32->bfloat16 rounding, exact
+integer brute force, closed forms, and the plain dequantise-then-matmul definition computed by
+numpy.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dg_oracle.cpp")
+_LIB = os.path.join(_HERE, "libdg_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``dg_oracle.cpp`` into ``libdg_oracle.so`` (g++, -ffp-contract=off, no -march)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-pthread", _SRC, "-o", tmp])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64 = ctypes.c_int, ctypes.c_int64
+        lib.dgo_e4m3_decode.restype = ctypes.c_double
+        lib.dgo_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.dgo_bf16_from_f64.restype = ctypes.c_uint16
+        lib.dgo_bf16_from_f64.argtypes = [ctypes.c_double]
+        lib.dgo_bf16_from_f64_array.argtypes = [P, P, i64]
+        lib.dgo_gemm_nt.argtypes = [P, P, i64, P, P, i32, i32, i32, P, P, i32]
+        lib.dgo_grouped_contiguous.restype = i32
+        lib.dgo_grouped_contiguous.argtypes = [P, P, i64, P, P, P, i32, i32, i32, i32, P, P, i32]
+        lib.dgo_grouped_masked.restype = i32
+        lib.dgo_grouped_masked.argtypes = [P, P, i64, P, P, P, i32, i32, i32, i32, P, P, i32]
+        lib.dgo_gemm_nt_sampled.argtypes = [P, P, i64, P, P, i32, i32, i32, i64, P, P, P, i32]
+        lib.dgo_hardware_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def hardware_threads() -> int:
+    return int(_load().dgo_hardware_threads())
+
+
+def _threads(threads):
+    return int(threads) if threads else hardware_threads()
+
+
+def _p(a: np.ndarray):
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("oracle inputs must be C-contiguous")
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u8(a):
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """FP64 value of each E4M3 byte (OCP definition)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.dgo_e4m3_decode(int(c)) for c in codes.ravel()], dtype=np.float64).reshape(codes.shape)
+
+
+def bf16_from_f64(x) -> np.ndarray:
+    """BF16 bit patterns (uint16) of FP64 values, rounded to nearest-even directly from FP64."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().dgo_bf16_from_f64_array(_p(x), _p(out), x.size)
+    return out
+
+
+def gemm_nt(A, sA, B, sB, threads=None, want_ref64=True, want_bf16=True):
+    """Dense D = A·Bᵀ. A[M,K] u8, sA[ceil(K/128)][ldsa] f32, B[N,K] u8, sB[ceil(N/128)][ceil(K/128)].
+
+    Returns (ref64 [M,N] float64 or None, D [M,N] uint16 BF16 bits or None)."""
+    A, B, sA, sB = _u8(A), _u8(B), _f32(sA), _f32(sB)
+    if B.ndim == 3:
+        B, sB = B[0], sB[0]
+    M, K = A.shape
+    N = B.shape[0]
+    ref = np.zeros((M, N), np.float64) if want_ref64 else None
+    D = np.zeros((M, N), np.uint16) if want_bf16 else None
+    _load().dgo_gemm_nt(_p(A), _p(sA), sA.shape[-1], _p(B), _p(sB), M, N, K,
+                        _p(ref) if ref is not None else None, _p(D) if D is not None else None,
+                        _threads(threads))
+    return ref, D
+
+
+def grouped_contiguous(A, sA, B, sB, m_indices, ref64_init=None, D_init=None, threads=None):
+    """Contiguous grouped D. Rows whose m_indices is -1 (or invalid) keep the initial contents.
+
+    Returns (ref64, D, n_invalid_rows)."""
+    A, B, sA, sB = _u8(A), _u8(B), _f32(sA), _f32(sB)
+    m_indices = np.ascontiguousarray(m_indices, dtype=np.int32)
+    M, K = A.shape
+    G, N, _ = B.shape
+    ref = np.array(ref64_init, dtype=np.float64, copy=True) if ref64_init is not None else np.zeros((M, N), np.float64)
+    D = np.array(D_init, dtype=np.uint16, copy=True) if D_init is not None else np.zeros((M, N), np.uint16)
+    bad = _load().dgo_grouped_contiguous(_p(A), _p(sA), sA.shape[-1], _p(B), _p(sB), _p(m_indices),
+                                         M, N, K, G, _p(ref), _p(D), _threads(threads))
+    return ref, D, int(bad)
+
+
+def grouped_masked(A, sA, B, sB, masked_m, ref64_init=None, D_init=None, threads=None):
+    """Masked grouped D[G,M_max,N]: rows m >= masked_m[g] keep the initial contents.
+
+    Returns (ref64, D, n_clamped_groups)."""
+    A, B, sA, sB = _u8(A), _u8(B), _f32(sA), _f32(sB)
+    masked_m = np.ascontiguousarray(masked_m, dtype=np.int32)
+    G, M_max, K = A.shape
+    N = B.shape[1]
+    ref = np.array(ref64_init, dtype=np.float64, copy=True) if ref64_init is not None else np.zeros((G, M_max, N), np.float64)
+    D = np.array(D_init, dtype=np.uint16, copy=True) if D_init is not None else np.zeros((G, M_max, N), np.uint16)
+    bad = _load().dgo_grouped_masked(_p(A), _p(sA), sA.shape[-1], _p(B), _p(sB), _p(masked_m),
+                                     G, M_max, N, K, _p(ref), _p(D), _threads(threads))
+    return ref, D, int(bad)
+
+
+def gemm_nt_sampled(A, sA, B, sB, ms, ns, threads=None) -> np.ndarray:
+    """FP64 values of the elements (ms[i], ns[i]) of a dense D = A·Bᵀ."""
+    A, B, sA, sB = _u8(A), _u8(B), _f32(sA), _f32(sB)
+    if B.ndim == 3:
+        B, sB = B[0], sB[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    out = np.empty(len(ms), np.float64)
+    M, K = A.shape
+    _load().dgo_gemm_nt_sampled(_p(A), _p(sA), sA.shape[-1], _p(B), _p(sB), M, B.shape[0], K,
+                                len(ms), _p(ms), _p(ns), _p(out), _threads(threads))
+    return out
+
+
+def contiguous_sampled(A, sA, B, sB, m_indices, ms, ns, threads=None) -> np.ndarray:
+    """FP64 values of sampled elements of a contiguous grouped problem (rows must be valid)."""
+    m_indices = np.asarray(m_indices)
+    ms = np.asarray(ms, np.int64)
+    ns = np.asarray(ns, np.int64)
+    out = np.empty(len(ms), np.float64)
+    groups = m_indices[ms]
+    for g in np.unique(groups):
+        sel = np.nonzero(groups == g)[0]
+        out[sel] = gemm_nt_sampled(A, sA, B[g], sB[g], ms[sel], ns[sel], threads)
+    return out
+
+
+def masked_sampled(A, sA, B, sB, gs, ms, ns, threads=None) -> np.ndarray:
+    """FP64 values of sampled elements (g, m, n) of a masked grouped problem."""
+    gs = np.asarray(gs, np.int64)
+    ms = np.asarray(ms, np.int64)
+    ns = np.asarray(ns, np.int64)
+    out = np.empty(len(ms), np.float64)
+    for g in np.unique(gs):
+        sel = np.nonzero(gs == g)[0]
+        out[sel] = gemm_nt_sampled(A[g], sA[g], B[g], sB[g], ms[sel], ns[sel], threads)
+    return out
