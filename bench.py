@@ -1,0 +1,460 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 (E4M3) fine-grained-scaled GEMM on GB300.
+
+Workload (one "step"): the dense FP8 GEMM sweep — M in {64, 128, 4096} x (N, K) in {(2112, 7168),
+(24576, 1536), (32768, 512), (7168, 16384), (4096, 7168), (7168, 2048)}, A[M,K] and B[N,K] drawn
+N(0,1) from seed 0 and quantised to E4M3 (1x128 A scales, 128x128 B scales, amax/448), BF16 D.
+Each of the 18 GEMMs is one launch of the sm_103a kernel through the C ABI; an L2 flush (a write
+of a 256 MB buffer) precedes every GEMM and lies outside the CUDA events that time it.
+
+Metric: useful TFLOP/s = sum(2*M*N*K) / sum(GEMM time). Printed as one JSON line with the
+roofline of the dominant kernel, the CPU oracle baseline, the end-to-end number through host
+buffers, the SM clocks seen during the timed region and the number of kernel launches.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the same sweep on its own GPU (replicas,
+weak scaling); rank 0 prints the whole-job throughput using the slowest rank's time.
+``--impl reference`` times the CPU oracle (the only reference this method has) on a bounded sample
+of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+SWEEP_NK = [(2112, 7168), (24576, 1536), (32768, 512), (7168, 16384), (4096, 7168), (7168, 2048)]
+SWEEP_M = [64, 128, 4096]
+SHAPES = [(M, N, K) for M in SWEEP_M for (N, K) in SWEEP_NK]
+WORKLOAD = "dense FP8 E4M3 GEMM sweep, M in {64,128,4096} x (N,K) in {(2112,7168),(24576,1536),(32768,512),(7168,16384),(4096,7168),(7168,2048)}"
+METRIC = "FP8 TFLOPS (2MNK/s) per shape; % of GB300 FP8 dense peak or HBM GB/s"
+L2_FLUSH_BYTES = 256 << 20
+CPU_SAMPLE_PER_SHAPE = 32768
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=CPU_SAMPLE_PER_SHAPE)
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def algorithmic_bytes(M, N, K):
+    nkb, nnb = -(-K // 128), -(-N // 128)
+    return M * K + N * K + 4 * M * nkb + 4 * nnb * nkb + 2 * M * N
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------------------------------
+# Inputs
+
+
+def make_inputs():
+    import dg_inputs
+    a_cache, b_cache, out = {}, {}, []
+    for (M, N, K) in SHAPES:
+        if (M, K) not in a_cache:
+            a_cache[(M, K)] = dg_inputs.make_a(M, K, seed=0)
+        if (N, K) not in b_cache:
+            b_cache[(N, K)] = dg_inputs.make_b(1, N, K, seed=0)
+        out.append((M, N, K, a_cache[(M, K)], b_cache[(N, K)]))
+    return out
+
+
+# ---------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self._thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        window = [s for (t, s) in self.samples if t0 <= t <= t1]
+        if not window and self.samples:   # a very short timed region: take the samples around it
+            window = [min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[1]]
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in window if num(s[0]) is not None]
+        smax = [num(s[1]) for s in window if num(s[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in window:
+            for name, v in zip(names, s[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(window),
+                "power_w_max": max((num(s[2]) or 0.0) for s in window)}
+
+
+def gpu_id_for_smi(device_index: int) -> str:
+    import torch
+    try:
+        props = torch.cuda.get_device_properties(device_index)
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", None)
+        dev = getattr(props, "pci_device_id", None)
+        if bus is not None and dom is not None and dev is not None:
+            return f"{dom:08x}:{bus:02x}:{dev:02x}.0"
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[device_index]
+    return str(device_index)
+
+
+# ---------------------------------------------------------------------------------------------
+# Our arm
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import moe_grouped_gemm_e4m3_gb300 as dg
+
+    torch.cuda.set_device(local)
+    dg.load()
+    pg = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = tdist
+
+    problems = make_inputs()
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    tensors = []
+    for (M, N, K, a, b) in problems:
+        tensors.append(dict(M=M, N=N, K=K, A=dev(a.A), sA=dev(a.sA), B=dev(b.B[0]), sB=dev(b.sB[0]),
+                            D=torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
+                            cfg=dg.dg_query_config(0, M, N, K)))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one_step(events):
+        for i, t in enumerate(tensors):
+            flush.fill_(i & 0xFF)
+            if events is not None:
+                events[i][0].record(stream)
+            dg.dg_fp8_gemm_nt(t["A"], t["sA"], t["B"], t["sB"], t["D"], stream)
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step(None)
+    torch.cuda.synchronize()
+    status = dg.dg_get_device_status()
+    if status:
+        raise RuntimeError(f"device status 0x{status:x} after warm-up")
+
+    sampler = ClockSampler(gpu_id_for_smi(local)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in tensors]
+          for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for s in range(args.steps):
+        one_step(ev[s])
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if pg:
+        pg.barrier()
+    if sampler:
+        time.sleep(0.1)
+        sampler.stop()
+    per_shape_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(len(tensors))]
+                             for s in range(args.steps)])   # [steps, shapes]
+    ms_per_step_local = float(per_shape_ms.sum(axis=1).mean())
+    ms_per_step = ms_per_step_local
+    if pg:
+        x = torch.tensor([ms_per_step_local], dtype=torch.float64, device="cuda")
+        pg.all_reduce(x, op=pg.ReduceOp.MAX)
+        ms_per_step = float(x.item())
+    status = dg.dg_get_device_status()
+    if status:
+        raise RuntimeError(f"device status 0x{status:x} after the timed region")
+
+    flops_step = sum(2.0 * t["M"] * t["N"] * t["K"] for t in tensors)
+    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+
+    # e2e through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(dg, problems, args, stream)
+        if pg:
+            x = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
+            pg.all_reduce(x, op=pg.ReduceOp.MAX)
+            e2e["value"] = world * flops_step / (float(x.item()) * 1e-3) / 1e12
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]           # dense FP8 = 2x dense BF16 (nominal ratio)
+    mean_ms = per_shape_ms.mean(axis=0)
+    per_shape = []
+    for i, t in enumerate(tensors):
+        M, N, K = t["M"], t["N"], t["K"]
+        tflops = 2.0 * M * N * K / (mean_ms[i] * 1e-3) / 1e12
+        gbs = algorithmic_bytes(M, N, K) / (mean_ms[i] * 1e-3) / 1e9
+        t_tc = 2.0 * M * N * K / (fp8_peak * 1e12)
+        t_hbm = algorithmic_bytes(M, N, K) / (peaks["hbm_gbs"] * 1e9)
+        bound = "tensor" if t_tc >= t_hbm else "hbm"
+        frac = (tflops / fp8_peak) if bound == "tensor" else (gbs / peaks["hbm_gbs"])
+        per_shape.append({"M": M, "N": N, "K": K, "us": round(float(mean_ms[i]) * 1e3, 2), "tflops": round(tflops, 1),
+                          "gbs": round(gbs, 1), "bound": bound, "roof_frac": round(frac, 3),
+                          "block_n": t["cfg"]["block_n"], "splits": t["cfg"]["splits"]})
+    # dominant kernel: the instantiation (tile width, split-K or not) with the largest share of time
+    groups = {}
+    for i, t in enumerate(tensors):
+        key = (t["cfg"]["block_n"], t["cfg"]["splits"] > 1)
+        g = groups.setdefault(key, {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0})
+        g["ms"] += float(mean_ms[i])
+        g["flops"] += 2.0 * t["M"] * t["N"] * t["K"]
+        g["bytes"] += algorithmic_bytes(t["M"], t["N"], t["K"])
+        g["launches"] += 1
+    dom_key = max(groups, key=lambda k: groups[k]["ms"])
+    dom = groups[dom_key]
+    tc_time = dom["flops"] / (fp8_peak * 1e12)
+    hbm_time = dom["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if tc_time >= hbm_time:
+        achieved = dom["flops"] / (dom["ms"] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / fp8_peak, 4)}
+    else:
+        achieved = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    roof.update({"traffic": None, "kernel": f"fp8_gemm_kernel<BN={dom_key[0]},{'split-K' if dom_key[1] else 'no split'},dense,bf16>",
+                 "launches_per_step": dom["launches"], "share_of_step": round(dom["ms"] / float(mean_ms.sum()), 3),
+                 "peak_source": f"{peaks['source']}: 2 x bf16_tflops (dense FP8 = 2x BF16 nominal)"})
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(problems, args.cpu_sample)
+
+    clocks = sampler.summary(t0, t1) if sampler else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate (fine-grained scales) -> bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shapes": len(tensors), "seed": 0, "values": "N(0,1)",
+                   "quantisation": "E4M3, A 1x128 / B 128x128 FP32 scales, amax/448",
+                   "l2": "256 MB write before every GEMM, outside the GEMM's CUDA events",
+                   "parallelism": f"replicas x{world}", "wall_ms_per_step": round((t1 - t0) * 1e3 / args.steps, 4)},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": ({k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")} if e2e else None),
+        "clocks": clocks,
+        "gpu_launches": len(tensors) * args.steps,
+        "per_shape": per_shape,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def measure_e2e(dg, problems, args, stream):
+    """Same sweep through host buffers: H2D of A, sA, B, sB from pinned memory, the GEMM, and the
+    D2H of D, all inside the timed region."""
+    import torch
+    host = []
+    h2d = d2h = 0
+    for (M, N, K, a, b) in problems:
+        h = dict(M=M, N=N, K=K)
+        for name, arr in (("A", a.A), ("sA", a.sA), ("B", b.B[0]), ("sB", b.sB[0])):
+            ht = torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
+            h[name] = ht
+            h["d" + name] = torch.empty_like(ht, device="cuda")
+            h2d += ht.numel() * ht.element_size()
+        h["dD"] = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        h["D"] = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+        d2h += M * N * 2
+        host.append(h)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    steps = max(3, min(args.steps, 10))
+
+    def one_step(evs):
+        for i, h in enumerate(host):
+            flush.fill_(i & 0xFF)
+            if evs is not None:
+                evs[i][0].record(stream)
+            for name in ("A", "sA", "B", "sB"):
+                h["d" + name].copy_(h[name], non_blocking=True)
+            dg.dg_fp8_gemm_nt(h["dA"], h["dsA"], h["dB"], h["dsB"], h["dD"], stream)
+            h["D"].copy_(h["dD"], non_blocking=True)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    one_step(None)
+    one_step(None)
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in host]
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s in range(steps):
+        one_step(ev[s])
+    torch.cuda.synchronize()
+    ms = float(np.mean([sum(e[0].elapsed_time(e[1]) for e in ev[s]) for s in range(steps)]))
+    flops = sum(2.0 * h["M"] * h["N"] * h["K"] for h in host)
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle (baseline and the reference arm)
+
+
+def cpu_sample_plan(problems, per_shape, seed=0):
+    rng = np.random.default_rng(seed)
+    plan = []
+    for (M, N, K, a, b) in problems:
+        ms = rng.integers(0, M, per_shape)
+        ns = rng.integers(0, N, per_shape)
+        plan.append((M, N, K, a, b, ms, ns))
+    return plan
+
+
+def cpu_baseline(problems, per_shape):
+    import oracle
+    plan = cpu_sample_plan(problems, per_shape)
+    threads = oracle.hardware_threads()
+    flops = 0.0
+    t0 = time.perf_counter()
+    for (M, N, K, a, b, ms, ns) in plan:
+        oracle.gemm_nt_sampled(a.A, a.sA, b.B[0], b.sB[0], ms, ns, threads=threads)
+        flops += 2.0 * K * len(ms)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{per_shape} random output elements of each of the {len(plan)} sweep GEMMs "
+                      f"({flops / 1e9:.2f} GFLOP, {dt:.1f} s), FP64 two-level accumulation, std::thread"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    problems = make_inputs()
+    threads = oracle.hardware_threads()
+    per_shape = max(64, args.cpu_sample // 8)
+    plan = cpu_sample_plan(problems, per_shape, seed=1)
+
+    def one_step():
+        fl = 0.0
+        for (M, N, K, a, b, ms, ns) in plan:
+            oracle.gemm_nt_sampled(a.A, a.sA, b.B[0], b.sB[0], ms, ns, threads=threads)
+            fl += 2.0 * K * len(ms)
+        return fl
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += one_step()
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shapes": len(plan), "seed": 0, "values": "N(0,1)",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {per_shape} random output elements of each of the {len(plan)} sweep "
+                                   f"GEMMs ({flops / args.steps / 1e9:.3f} GFLOP)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

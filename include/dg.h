@@ -1,0 +1,160 @@
+/*
+ * dg.h — C ABI of libdg: FP8 (E4M3) GEMM D = A·Bᵀ with DeepSeek-V3 fine-grained scaling on
+ * GB300 (sm_103a), in its dense form and the two MoE grouped forms.
+ *
+ * What the calls compute (sources are the DeepGEMM pages; the scale granularity is from the
+ * DeepSeek-V3 Technical Report, § 3.3.2 "Fine-Grained Quantization"):
+ *
+ *   D[m,n] = Σ_kb  sA[m,kb] · sB[n/128,kb] · Σ_{k in kb} A[m,k]·B[n,k]        kb = k/128
+ *
+ * - "NT" naming and layout: fp8_gemm_nt computes D = C + A @ B.T, A row-major, B col-major
+ *   ("DeepGEMM: İnce ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri",
+ *   tr.news.hada.io/topic?id=19459, § "GEMM arayüzü ve yerleşim kısıtları"). C is absent: D is
+ *   overwritten.
+ * - The per-128-K partial is promoted into an FP32 accumulator after the scales are applied
+ *   (two-level accumulation on CUDA cores: "DeepGEMM" first-release summary,
+ *   tr.news.hada.io/topic?id=19444, feature list).
+ * - The LHS scaling factor is TMA-aligned and transposed (same page as the NT naming, same
+ *   section), i.e. MN-major.
+ *
+ * Common conventions for every GEMM entry point:
+ * - Pointers: all tensor pointers are DEVICE memory owned by the caller. libdg keeps no pointer
+ *   after the call returns. Calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *   legacy default stream) and never synchronise.
+ * - A: E4M3 bytes, row-major [rows, K] (K contiguous). B: E4M3 bytes, [G, N, K] (K contiguous;
+ *   dense G = 1). E4M3 is the OCP FP8 format (bias 7, 0x7F/0xFF NaN, max 448).
+ * - sA: FP32, MN-major: sA[kb * ldsa + m] with ldsa = dg_get_tma_aligned_size(rows, 4)
+ *   (rows rounded up to a multiple of 4), kb in [0, ceil(K/128)).
+ * - sB: FP32, sB[(g * ceil(N/128) + nb) * ceil(K/128) + kb], one scale per 128x128 block.
+ * - D: row-major [rows, N]; BF16 bit patterns (uint16_t) rounded to nearest-even, or FP32 for
+ *   the *_f32 variants. The *_f32 variants run the same kernel with the same tile
+ *   configuration and accumulation order and store the FP32 accumulator instead of rounding it:
+ *   D_bf16 == RNE(D_f32) element by element.
+ * - Alignment (TMA: 16-byte global strides and addresses): K % 16 == 0, N % 8 == 0 (BF16 D) or
+ *   N % 4 == 0 (FP32 D); A, B and D 16-byte aligned; sA, sB 4-byte aligned.
+ *   Violations return DG_ERR_ALIGNMENT or DG_ERR_INVALID_ARG and launch nothing.
+ * - Empty problems (a zero M/N/G) return DG_OK and launch nothing.
+ * - Errors found on the device (a group index out of range, masked_m outside [0, M_max], a
+ *   pipeline wait that timed out) never trap: the kernel skips the affected rows or tiles, sets
+ *   bits of a device status word and returns. Read it with dg_get_device_status().
+ * - Split-K: for small problems the library may split K across CTAs and reduce the FP32
+ *   partials in a fixed order (deterministic). Its workspace is a library-owned buffer per
+ *   device, allocated on the first call that needs it and grown when a larger one is needed
+ *   (that call allocates; make it before any CUDA-graph capture). Calls that use the workspace
+ *   and overlap on the GPU (different streams of one device) race on it.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad G */
+  DG_ERR_ALIGNMENT = 2,      /* K % 16, N % 8 (N % 4 for FP32 D), or pointer alignment */
+  DG_ERR_UNSUPPORTED = 3,    /* no GB300-class device, or a size beyond a documented limit */
+  DG_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed; see dg_last_error_string() */
+  DG_ERR_DEVICE_STATUS = 5   /* dg_get_device_status() found a non-zero device status word */
+} dg_status;
+
+/* Bits of the device status word. */
+#define DG_DEV_BAD_GROUP_INDEX 0x1  /* contiguous: m_indices[m] >= G or < -1, or two groups in one 128-row block */
+#define DG_DEV_BAD_MASKED_M 0x2     /* masked: masked_m[g] < 0 or > M_max (clamped) */
+#define DG_DEV_TIMEOUT 0x4          /* a pipeline wait exceeded its time limit; the kernel abandoned the work */
+
+typedef void* dg_stream_t; /* cudaStream_t */
+
+/*
+ * Dense GEMM: D[M,N] = A[M,K]·B[N,K]ᵀ with fine-grained scales.
+ * Source: fp8_gemm_nt ("DeepGEMM: İnce ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri",
+ * tr.news.hada.io/topic?id=19459, § "GEMM arayüzü ve yerleşim kısıtları" and § "Dense ve Grouped
+ * GEMM").
+ *   A  [M,K] E4M3          sA [ceil(K/128)][align4(M)] FP32 (MN-major)
+ *   B  [N,K] E4M3          sB [ceil(N/128)][ceil(K/128)] FP32
+ *   D  [M,N] BF16 bits
+ */
+dg_status dg_fp8_gemm_nt(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                         uint16_t* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_nt_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                             float* D, int M, int N, int K, dg_stream_t stream);
+
+/*
+ * Contiguous-layout grouped GEMM: grouped along M only; N and K are shared by the G groups
+ * (experts). The experts' token rows are concatenated into one A, and each expert's segment is
+ * aligned to the GEMM M block, dg_get_mk_alignment_for_contiguous_layout() = 128 rows.
+ * Source: tr.news.hada.io/topic?id=19459, § "Dense ve Grouped GEMM"; first-release summary
+ * tr.news.hada.io/topic?id=19444, § "MoE modelleri için gruplanmış GEMM performansı".
+ *   A  [M_total,K] E4M3     sA [ceil(K/128)][align4(M_total)]
+ *   B  [G,N,K] E4M3         sB [G][ceil(N/128)][ceil(K/128)]
+ *   m_indices [M_total] int32 on the device: the group of each row, or -1 for a padding row.
+ *             Every 128-row block must hold one group (plus -1 rows). Padding rows of D are
+ *             left untouched; an all-padding block is skipped without reading B. An index
+ *             >= G or < -1 sets DG_DEV_BAD_GROUP_INDEX and leaves that row (or block) untouched.
+ *   D  [M_total,N] BF16 bits
+ */
+dg_status dg_fp8_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                    const int32_t* m_indices, uint16_t* D, int M_total, int N, int K,
+                                    int G, dg_stream_t stream);
+dg_status dg_fp8_grouped_contiguous_f32(const uint8_t* A, const float* sA, const uint8_t* B,
+                                        const float* sB, const int32_t* m_indices, float* D,
+                                        int M_total, int N, int K, int G, dg_stream_t stream);
+
+/*
+ * Masked-layout grouped GEMM (MoE decode under CUDA graphs: the CPU does not know how many
+ * tokens each expert received, so the counts are read on the device and only the valid rows are
+ * computed). Source: tr.news.hada.io/topic?id=19459, § "Dense ve Grouped GEMM"
+ * (m_grouped_fp8_gemm_nt_masked); tr.news.hada.io/topic?id=19444, § "MoE modelleri için
+ * gruplanmış GEMM performansı".
+ *   A  [G,M_max,K] E4M3     sA [G][ceil(K/128)][align4(M_max)]
+ *   B  [G,N,K] E4M3         sB [G][ceil(N/128)][ceil(K/128)]
+ *   masked_m [G] int32 on the device: valid rows of each group. Rows m >= masked_m[g] of D are
+ *             never written; a group with masked_m[g] == 0 reads neither A nor B. Values outside
+ *             [0, M_max] are clamped and set DG_DEV_BAD_MASKED_M.
+ *   D  [G,M_max,N] BF16 bits
+ * The host never reads masked_m, so the call can be captured in a CUDA graph.
+ */
+dg_status dg_fp8_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                const int32_t* masked_m, uint16_t* D, int G, int M_max, int N, int K,
+                                dg_stream_t stream);
+dg_status dg_fp8_grouped_masked_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                    const int32_t* masked_m, float* D, int G, int M_max, int N, int K,
+                                    dg_stream_t stream);
+
+/* x rounded up so that x * elem_bytes is a multiple of 16 bytes (the TMA alignment).
+   Source: get_tma_aligned_size, tr.news.hada.io/topic?id=19459, § "Yardımcı fonksiyonlar ve
+   ortam değişkenleri". Returns -1 for x < 0 or elem_bytes not in {1, 2, 4, 8, 16}. */
+int dg_get_tma_aligned_size(int x, int elem_bytes);
+
+/* Row alignment of each group's segment in the contiguous layout (128, the M block).
+   Source: get_mk_alignment_for_contiguous_layout, same page and section. */
+int dg_get_mk_alignment_for_contiguous_layout(void);
+
+/* Cap on the SMs the kernels use (0 restores the device's SM count; the environment variable
+   DG_NUM_SMS sets the initial cap). Source: set_num_sms / get_num_sms, same page and section.
+   dg_get_num_sms() returns the cap in force for the current device. */
+void dg_set_num_sms(int n);
+int dg_get_num_sms(void);
+
+/* Reads and clears the device status word of the current device after synchronising `stream`.
+   *code receives the DG_DEV_* bits. Returns DG_ERR_DEVICE_STATUS when a bit was set. */
+dg_status dg_get_device_status(int* code, dg_stream_t stream);
+
+/* Message describing the last error returned by a call on this thread ("" if none). */
+const char* dg_last_error_string(void);
+
+/* The tile configuration a GEMM call with these arguments would launch, for logging and tests.
+   mode: 0 dense, 1 contiguous, 2 masked; out_f32: 0 or 1. Writes 6 ints to cfg:
+   {block_m, block_n, stages, splits, grid, num_tiles_upper_bound}. Setting the environment
+   variable DG_PRINT_CONFIGS=1 prints the same per call on stderr. */
+dg_status dg_query_config(int mode, int M, int N, int K, int G, int out_f32, int* cfg);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H */

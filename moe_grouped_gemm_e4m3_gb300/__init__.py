@@ -1,0 +1,224 @@
+"""FP8 (E4M3) fine-grained-scaled GEMM for GB300 — thin Python binding of libdg (include/dg.h).
+
+Argument marshalling only: every step of the GEMM runs in the sm_103a kernels of ``libdg.so``.
+PyTorch supplies device memory and the current CUDA stream. There is no fallback: if the library
+is missing or cannot load, every call raises.
+
+The names mirror the C ABI:
+
+* ``dg_fp8_gemm_nt(A, sA, B, sB, D)``                       dense D = A·Bᵀ
+* ``dg_fp8_grouped_contiguous(A, sA, B, sB, m_indices, D)``  M-grouped, contiguous layout
+* ``dg_fp8_grouped_masked(A, sA, B, sB, masked_m, D)``       M-grouped, masked layout
+* ``*_f32`` variants store the FP32 accumulator instead of BF16 (same kernel and order).
+
+Tensor contract (all CUDA, contiguous): A uint8/float8_e4m3fn [rows, K] (masked: [G, M_max, K]);
+B uint8/float8_e4m3fn [N, K] or [G, N, K]; sA float32 MN-major [ceil(K/128), align4(rows)]
+(masked: [G, ceil(K/128), align4(M_max)]); sB float32 [G, ceil(N/128), ceil(K/128)]; D bfloat16
+(or float32) [rows, N] (masked: [G, M_max, N]); m_indices / masked_m int32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build_mod
+
+__all__ = [
+    "DGError", "load", "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_grouped_contiguous",
+    "dg_fp8_grouped_contiguous_f32", "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32",
+    "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms",
+    "dg_get_num_sms", "dg_get_device_status", "dg_last_error_string", "dg_query_config",
+    "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
+    "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
+    "DG_DEV_TIMEOUT",
+]
+
+DG_OK, DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_DEVICE_STATUS = range(6)
+DG_DEV_BAD_GROUP_INDEX, DG_DEV_BAD_MASKED_M, DG_DEV_TIMEOUT = 0x1, 0x2, 0x4
+
+# Every symbol include/dg.h declares (checked against the built library by the CPU tests).
+EXPORTED_SYMBOLS = (
+    "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32",
+    "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_get_tma_aligned_size",
+    "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms", "dg_get_num_sms", "dg_get_device_status",
+    "dg_last_error_string", "dg_query_config",
+)
+
+
+class DGError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"libdg status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(build_if_missing: bool = True):
+    """Loads libdg.so (building it first if it is missing or stale and nvcc is available)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build_mod.LIB
+    if build_if_missing and not _build_mod.up_to_date():
+        _build_mod.build()
+    if not os.path.exists(path):
+        raise DGError(DG_ERR_UNSUPPORTED, f"libdg.so not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, i32 = ctypes.c_void_p, ctypes.c_int
+    for name in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i32, [P, P, P, P, P, i32, i32, i32, P]
+    for name in ("dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
+    for name in ("dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
+    lib.dg_get_tma_aligned_size.restype, lib.dg_get_tma_aligned_size.argtypes = i32, [i32, i32]
+    lib.dg_get_mk_alignment_for_contiguous_layout.restype = i32
+    lib.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
+    lib.dg_set_num_sms.restype, lib.dg_set_num_sms.argtypes = None, [i32]
+    lib.dg_get_num_sms.restype, lib.dg_get_num_sms.argtypes = i32, []
+    lib.dg_get_device_status.restype, lib.dg_get_device_status.argtypes = i32, [ctypes.POINTER(i32), P]
+    lib.dg_last_error_string.restype, lib.dg_last_error_string.argtypes = ctypes.c_char_p, []
+    lib.dg_query_config.restype = i32
+    lib.dg_query_config.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != DG_OK:
+        raise DGError(status, load().dg_last_error_string().decode(errors="replace"))
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t, name, dtypes):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _fp8_types():
+    import torch
+    return (torch.uint8, torch.float8_e4m3fn)
+
+
+def _f32():
+    import torch
+    return (torch.float32,)
+
+
+def _d_types(f32: bool):
+    import torch
+    return (torch.float32,) if f32 else (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def _dense(name, f32, A, sA, B, sB, D, stream):
+    lib = load()
+    M, K = A.shape
+    N = B.shape[-2]
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", _f32()), _ptr(D, "D", _d_types(f32)), M, N, K, _stream(stream)))
+    return D
+
+
+def dg_fp8_gemm_nt(A, sA, B, sB, D, stream=None):
+    """D[M,N] (bfloat16) = A[M,K]·B[N,K]ᵀ with fine-grained scales."""
+    return _dense("dg_fp8_gemm_nt", False, A, sA, B, sB, D, stream)
+
+
+def dg_fp8_gemm_nt_f32(A, sA, B, sB, D, stream=None):
+    """As dg_fp8_gemm_nt, storing the FP32 accumulator."""
+    return _dense("dg_fp8_gemm_nt_f32", True, A, sA, B, sB, D, stream)
+
+
+def _contig(name, f32, A, sA, B, sB, m_indices, D, stream):
+    import torch
+    lib = load()
+    M, K = A.shape
+    G, N = B.shape[0], B.shape[1]
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", _f32()), _ptr(m_indices, "m_indices", (torch.int32,)),
+                              _ptr(D, "D", _d_types(f32)), M, N, K, G, _stream(stream)))
+    return D
+
+
+def dg_fp8_grouped_contiguous(A, sA, B, sB, m_indices, D, stream=None):
+    """Contiguous-layout grouped GEMM: row m of D uses expert m_indices[m] (-1: padding, untouched)."""
+    return _contig("dg_fp8_grouped_contiguous", False, A, sA, B, sB, m_indices, D, stream)
+
+
+def dg_fp8_grouped_contiguous_f32(A, sA, B, sB, m_indices, D, stream=None):
+    return _contig("dg_fp8_grouped_contiguous_f32", True, A, sA, B, sB, m_indices, D, stream)
+
+
+def _masked(name, f32, A, sA, B, sB, masked_m, D, stream):
+    import torch
+    lib = load()
+    G, M_max, K = A.shape
+    N = B.shape[1]
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", _f32()), _ptr(masked_m, "masked_m", (torch.int32,)),
+                              _ptr(D, "D", _d_types(f32)), G, M_max, N, K, _stream(stream)))
+    return D
+
+
+def dg_fp8_grouped_masked(A, sA, B, sB, masked_m, D, stream=None):
+    """Masked-layout grouped GEMM: rows m < masked_m[g] of group g are computed, the rest untouched."""
+    return _masked("dg_fp8_grouped_masked", False, A, sA, B, sB, masked_m, D, stream)
+
+
+def dg_fp8_grouped_masked_f32(A, sA, B, sB, masked_m, D, stream=None):
+    return _masked("dg_fp8_grouped_masked_f32", True, A, sA, B, sB, masked_m, D, stream)
+
+
+def dg_get_tma_aligned_size(x: int, elem_bytes: int) -> int:
+    return int(load().dg_get_tma_aligned_size(x, elem_bytes))
+
+
+def dg_get_mk_alignment_for_contiguous_layout() -> int:
+    return int(load().dg_get_mk_alignment_for_contiguous_layout())
+
+
+def dg_set_num_sms(n: int) -> None:
+    load().dg_set_num_sms(int(n))
+
+
+def dg_get_num_sms() -> int:
+    return int(load().dg_get_num_sms())
+
+
+def dg_get_device_status(stream=None) -> int:
+    """Synchronises `stream`, reads and clears the device status word; returns its DG_DEV_* bits."""
+    code = ctypes.c_int(0)
+    st = load().dg_get_device_status(ctypes.byref(code), _stream(stream))
+    if st not in (DG_OK, DG_ERR_DEVICE_STATUS):
+        _check(st)
+    return int(code.value)
+
+
+def dg_last_error_string() -> str:
+    return load().dg_last_error_string().decode(errors="replace")
+
+
+def dg_query_config(mode: int, M: int, N: int, K: int, G: int = 1, out_f32: bool = False) -> dict:
+    """Tile configuration a call would launch: mode 0 dense, 1 contiguous, 2 masked."""
+    cfg = (ctypes.c_int * 6)()
+    _check(load().dg_query_config(mode, M, N, K, G, 1 if out_f32 else 0, cfg))
+    keys = ("block_m", "block_n", "stages", "splits", "grid", "tiles")
+    return dict(zip(keys, [int(v) for v in cfg]))

@@ -1,0 +1,417 @@
+// dg_api.cu — the C ABI of libdg (declared in include/dg.h): argument validation, tile
+// configuration, TMA descriptor encoding, the split-K workspace, the device status word and the
+// launch of the sm_103a kernels. No GEMM arithmetic happens on the host.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "dg.h"
+#include "dg_launch.h"
+
+static_assert(dg::kStatusTimeout == DG_DEV_TIMEOUT, "status bit mismatch");
+static_assert(dg::kStatusBadGroup == DG_DEV_BAD_GROUP_INDEX, "status bit mismatch");
+static_assert(dg::kStatusBadMaskedM == DG_DEV_BAD_MASKED_M, "status bit mismatch");
+
+// The device status word: one per device context, read and cleared by dg_get_device_status().
+__device__ int g_dg_device_status;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+dg_status fail(dg_status s, const std::string& msg) {
+  t_last_error = msg;
+  return s;
+}
+
+dg_status fail_cuda(cudaError_t e, const char* what) {
+  return fail(DG_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 16;
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  int* status = nullptr;      // device address of g_dg_device_status
+  float* workspace = nullptr; // split-K partial tiles
+  size_t workspace_floats = 0;
+  int* counters = nullptr;    // split-K arrival counters
+  size_t counter_count = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+std::atomic<int> g_num_sms_cap{-1};  // -1: not yet initialised from DG_NUM_SMS; 0: no cap
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+int num_sms_cap() {
+  int c = g_num_sms_cap.load();
+  if (c < 0) {
+    const char* env = std::getenv("DG_NUM_SMS");
+    int v = env ? std::atoi(env) : 0;
+    if (v < 0) v = 0;
+    int expected = -1;
+    g_num_sms_cap.compare_exchange_strong(expected, v);
+    c = g_num_sms_cap.load();
+  }
+  return c;
+}
+
+// State of the current device, initialised on first use.
+dg_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DG_ERR_UNSUPPORTED, "device ordinal beyond 64");
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail_cuda(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+      return fail(DG_ERR_UNSUPPORTED, "libdg is built for sm_103a (GB300); this device is sm_" +
+                                          std::to_string(major) + std::to_string(minor));
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_dg_device_status)) != cudaSuccess)
+      return fail_cuda(e, "cudaGetSymbolAddress(status)");
+    st.status = static_cast<int*>(p);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    st.ready = true;
+  }
+  *out = &st;
+  return DG_OK;
+}
+
+int effective_sms(const DeviceState& st) {
+  const int cap = num_sms_cap();
+  return (cap > 0 && cap < st.sm_count) ? cap : st.sm_count;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Tile configuration: a static heuristic keyed on the problem shape and the SM count.
+
+struct Config {
+  int block_n;
+  int stages;
+  int splits;
+  int kb_per_split;
+  int tiles;       // output tiles (masked: upper bound)
+  int grid;
+  int raster_m;
+};
+
+Config choose_config(int mode, int rows, int N, int K, int G, int num_sms) {
+  Config c{};
+  const int nkb = ceil_div(K, 128);
+  const int m_blocks = ceil_div(rows, 128) * (mode == dg::kMasked ? G : 1);
+  int bn = N > 128 ? 256 : 128;
+  int tiles = m_blocks * ceil_div(N, bn);
+  if (bn == 256 && tiles < num_sms) {  // too few wide tiles to fill the GPU: use narrow ones
+    bn = 128;
+    tiles = m_blocks * ceil_div(N, bn);
+  }
+  int splits = 1;
+  if (mode != dg::kMasked && tiles < num_sms) {
+    // Few tiles (small M): split K so that every SM streams operands; keep >= 2 K-blocks each.
+    splits = num_sms / tiles;
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    if (splits > nkb / 2) splits = nkb / 2;
+    if (splits < 1) splits = 1;
+  }
+  c.kb_per_split = ceil_div(nkb, splits);
+  c.splits = ceil_div(nkb, c.kb_per_split);
+  c.block_n = bn;
+  c.stages = dg::stages_for(bn);
+  c.tiles = tiles;
+  const long long units = (long long)tiles * c.splits;
+  c.grid = (int)(units < num_sms ? units : num_sms);
+  if (c.grid < 1) c.grid = 1;
+  const int mb = ceil_div(rows, 128);
+  c.raster_m = mb < 16 ? (mb > 0 ? mb : 1) : 16;
+  return c;
+}
+
+bool print_configs() {
+  static const bool on = [] {
+    const char* e = std::getenv("DG_PRINT_CONFIGS");
+    return e && std::atoi(e) != 0;
+  }();
+  return on;
+}
+
+// ---------------------------------------------------------------------------------------------
+// TMA descriptors
+
+dg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapL2promotion promo,
+                    const char* what) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DG_ERR_CUDA, std::string("cuTensorMapEncodeTiled(") + what + ") failed: " + std::to_string((int)r));
+  return DG_OK;
+}
+
+// Grows the split-K workspace of the device to at least `floats` partial values and `counters`
+// arrival counters (new counters are zeroed on `stream`).
+dg_status ensure_workspace(DeviceState& st, size_t floats, size_t counters, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  cudaError_t e;
+  if (st.workspace_floats < floats) {
+    if (st.workspace) cudaFree(st.workspace);
+    st.workspace = nullptr;
+    st.workspace_floats = 0;
+    if ((e = cudaMalloc(&st.workspace, floats * sizeof(float))) != cudaSuccess) return fail_cuda(e, "cudaMalloc(workspace)");
+    st.workspace_floats = floats;
+  }
+  if (st.counter_count < counters) {
+    if (st.counters) cudaFree(st.counters);
+    st.counters = nullptr;
+    st.counter_count = 0;
+    if ((e = cudaMalloc(&st.counters, counters * sizeof(int))) != cudaSuccess) return fail_cuda(e, "cudaMalloc(counters)");
+    if ((e = cudaMemsetAsync(st.counters, 0, counters * sizeof(int), stream)) != cudaSuccess)
+      return fail_cuda(e, "cudaMemsetAsync(counters)");
+    st.counter_count = counters;
+  }
+  return DG_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Common implementation of the six GEMM entry points.
+//   mode dense: rows = M, G = 1;  contiguous: rows = M_total;  masked: rows = M_max (per group).
+dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                   const int32_t* idx, void* D, int rows, int N, int K, int G, cudaStream_t stream) {
+  t_last_error.clear();
+  if (rows < 0 || N < 0 || K < 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
+  if (mode != dg::kDense && G < 1 && rows > 0) {
+    if (G == 0) return DG_OK;
+  }
+  if (rows == 0 || N == 0 || G == 0) return DG_OK;
+  if (K == 0) return fail(DG_ERR_INVALID_ARG, "K must be positive");
+  if (!A || !sA || !B || !sB || !D) return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
+  if (mode != dg::kDense && !idx) return fail(DG_ERR_INVALID_ARG, mode == dg::kMasked ? "null masked_m" : "null m_indices");
+  if (K % 16 != 0) return fail(DG_ERR_ALIGNMENT, "K must be a multiple of 16 (16-byte rows of E4M3 A and B)");
+  if (N % (out_f32 ? 4 : 8) != 0)
+    return fail(DG_ERR_ALIGNMENT, out_f32 ? "N must be a multiple of 4 (16-byte rows of FP32 D)"
+                                          : "N must be a multiple of 8 (16-byte rows of BF16 D)");
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16))
+    return fail(DG_ERR_ALIGNMENT, "A, B and D must be 16-byte aligned");
+  if (!aligned(sA, 4) || !aligned(sB, 4) || (idx && !aligned(idx, 4)))
+    return fail(DG_ERR_ALIGNMENT, "sA, sB and index tensors must be 4-byte aligned");
+  const long long rows_total = (long long)rows * (mode == dg::kMasked ? G : 1);
+  const long long b_rows = (long long)N * (mode == dg::kDense ? 1 : G);
+  if (rows_total > INT_MAX - 256 || b_rows > INT_MAX - 256 || K > INT_MAX - 256)
+    return fail(DG_ERR_UNSUPPORTED, "a tensor extent exceeds 2^31 - 257");
+
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  const int sms = effective_sms(*st);
+  const Config cfg = choose_config(mode, rows, N, K, mode == dg::kDense ? 1 : G, sms);
+  if ((long long)cfg.tiles * cfg.splits > INT_MAX / 2) return fail(DG_ERR_UNSUPPORTED, "too many tiles");
+
+  dg::LaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  dg::GemmParams& p = a.p;
+  p.M = rows;
+  p.N = N;
+  p.K = K;
+  p.G = mode == dg::kDense ? 1 : G;
+  p.nkb = ceil_div(K, 128);
+  p.nnb = ceil_div(N, 128);
+  p.ldsa = dg_get_tma_aligned_size(rows, 4);
+  p.num_m_blocks = ceil_div(rows, 128);
+  p.num_n_blocks = ceil_div(N, cfg.block_n);
+  p.num_splits = cfg.splits;
+  p.kb_per_split = cfg.kb_per_split;
+  p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles * cfg.splits;
+  p.raster_m = cfg.raster_m;
+  p.sA = sA;
+  p.sB = sB;
+  p.m_indices = mode == dg::kContiguous ? idx : nullptr;
+  p.masked_m = mode == dg::kMasked ? idx : nullptr;
+  p.D = D;
+  p.status = st->status;
+  if (cfg.splits > 1) {
+    const size_t floats = (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n;
+    if ((s = ensure_workspace(*st, floats, (size_t)cfg.tiles, stream)) != DG_OK) return s;
+    p.workspace = st->workspace;
+    p.counters = st->counters;
+  }
+
+  if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)K, (uint64_t)rows_total, (uint64_t)K, 128, 128,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
+    return s;
+  if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)b_rows, (uint64_t)K, 128,
+                     (uint32_t)cfg.block_n, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
+    return s;
+  if (out_f32) {
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)N, (uint64_t)rows_total, (uint64_t)N * 4, 32, 32,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D");
+  } else {
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)rows_total, (uint64_t)N * 2, 64, 32,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D");
+  }
+  if (s != DG_OK) return s;
+
+  a.block_n = cfg.block_n;
+  a.out_f32 = out_f32;
+  a.grid = cfg.grid;
+  a.stream = stream;
+  if (print_configs()) {
+    static const char* names[3] = {"dense", "contiguous", "masked"};
+    std::fprintf(stderr, "[dg] %s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d grid=%d tiles=%d\n",
+                 names[mode], out_f32 ? "/f32" : "", rows, N, K, p.G, cfg.block_n, cfg.stages, cfg.splits, cfg.grid,
+                 cfg.tiles);
+  }
+  cudaError_t e;
+  switch (mode) {
+    case dg::kDense: e = dg::launch_dense(a); break;
+    case dg::kContiguous: e = dg::launch_contiguous(a); break;
+    default: e = dg::launch_masked(a); break;
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dg_status dg_fp8_gemm_nt(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int M,
+                         int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_gemm_nt_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D, int M,
+                             int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_grouped_contiguous(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                    const int32_t* m_indices, uint16_t* D, int M_total, int N, int K, int G,
+                                    dg_stream_t stream) {
+  return run_gemm(dg::kContiguous, false, A, sA, B, sB, m_indices, D, M_total, N, K, G,
+                  static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_grouped_contiguous_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                        const int32_t* m_indices, float* D, int M_total, int N, int K, int G,
+                                        dg_stream_t stream) {
+  return run_gemm(dg::kContiguous, true, A, sA, B, sB, m_indices, D, M_total, N, K, G,
+                  static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_grouped_masked(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                const int32_t* masked_m, uint16_t* D, int G, int M_max, int N, int K,
+                                dg_stream_t stream) {
+  return run_gemm(dg::kMasked, false, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_grouped_masked_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                    const int32_t* masked_m, float* D, int G, int M_max, int N, int K,
+                                    dg_stream_t stream) {
+  return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream));
+}
+
+int dg_get_tma_aligned_size(int x, int elem_bytes) {
+  if (x < 0 || (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8 && elem_bytes != 16)) return -1;
+  const int per = 16 / elem_bytes;
+  return (x + per - 1) / per * per;
+}
+
+int dg_get_mk_alignment_for_contiguous_layout(void) { return 128; }
+
+void dg_set_num_sms(int n) {
+  num_sms_cap();  // make sure the environment default has been read first
+  g_num_sms_cap.store(n > 0 ? n : 0);
+}
+
+int dg_get_num_sms(void) {
+  DeviceState* st = nullptr;
+  if (device_state(&st) != DG_OK) {
+    const int cap = num_sms_cap();
+    return cap > 0 ? cap : 0;
+  }
+  return effective_sms(*st);
+}
+
+dg_status dg_get_device_status(int* code, dg_stream_t stream) {
+  t_last_error.clear();
+  if (!code) return fail(DG_ERR_INVALID_ARG, "null code");
+  *code = 0;
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  int v = 0;
+  if ((e = cudaMemcpy(&v, st->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail_cuda(e, "cudaMemcpy(status)");
+  if (v != 0) {
+    if ((e = cudaMemset(st->status, 0, sizeof(int))) != cudaSuccess) return fail_cuda(e, "cudaMemset(status)");
+    if ((v & DG_DEV_TIMEOUT) && st->counters) {
+      // an abandoned split-K tile can leave its arrival counter non-zero
+      std::lock_guard<std::mutex> lock(g_mutex);
+      if ((e = cudaMemset(st->counters, 0, st->counter_count * sizeof(int))) != cudaSuccess)
+        return fail_cuda(e, "cudaMemset(counters)");
+    }
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    *code = v;
+    return fail(DG_ERR_DEVICE_STATUS, "device status word 0x" + std::to_string(v));
+  }
+  return DG_OK;
+}
+
+const char* dg_last_error_string(void) { return t_last_error.c_str(); }
+
+dg_status dg_query_config(int mode, int M, int N, int K, int G, int out_f32, int* cfg) {
+  t_last_error.clear();
+  (void)out_f32;  // the configuration never depends on the output type
+  if (!cfg || mode < 0 || mode > 2 || M < 0 || N < 0 || K <= 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "bad query");
+  DeviceState* st = nullptr;
+  int sms = num_sms_cap();
+  if (device_state(&st) == DG_OK) sms = effective_sms(*st);
+  if (sms <= 0) sms = 152;  // no device: report the GB300 configuration
+  const Config c = choose_config(mode, M, N, K, mode == 0 ? 1 : G, sms);
+  cfg[0] = 128;
+  cfg[1] = c.block_n;
+  cfg[2] = c.stages;
+  cfg[3] = c.splits;
+  cfg[4] = c.grid;
+  cfg[5] = c.tiles;
+  return DG_OK;
+}
+
+}  // extern "C"

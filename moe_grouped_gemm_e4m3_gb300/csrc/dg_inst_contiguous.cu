@@ -1,0 +1,6 @@
+// dg_inst_contiguous.cu — instantiations of the GEMM kernel for the contiguous form (BN 128/256, BF16/FP32 D).
+#include "dg_launch.h"
+
+namespace dg {
+cudaError_t launch_contiguous(const LaunchArgs& a) { return launch_mode<kContiguous>(a); }
+}  // namespace dg

@@ -1,0 +1,576 @@
+// dg_kernel.cuh — the FP8 (E4M3) fine-grained-scaled GEMM kernel for GB300 (sm_103a).
+//
+// What it computes (DeepGEMM pages: "DeepGEMM: İnce ölçeklendirmeyle temiz ve verimli FP8 GEMM
+// çekirdekleri", tr.news.hada.io/topic?id=19459, § "GEMM arayüzü ve yerleşim kısıtları" and
+// § "Dense ve Grouped GEMM"; DeepSeek-V3 Technical Report § 3.3.2 for the scale granularity):
+//
+//     D[m,n] = Σ_kb sA[m,kb]·sB[n/128,kb]·P_kb[m,n],   P_kb = Σ_{k in 128-deep slice kb} A[m,k]·B[n,k]
+//
+// with P_kb produced by the tensor core and promoted, after scaling, into an FP32 accumulator on
+// CUDA cores (the two-level accumulation of the "DeepGEMM" first-release summary,
+// tr.news.hada.io/topic?id=19444, and "DeepSeek AI libera DeepGEMM", 7minutos.es, § "Detalles y
+// beneficios técnicos").
+//
+// GB300 design (one persistent CTA per SM, warp-specialised; the pages' Hopper design — wgmma,
+// register accumulators, FFMA yield-bit interleaving — is prior art, not the blueprint):
+//   * producer warp: TMA loads of 128x128-byte A tiles and BNx128-byte B tiles (128-byte swizzle)
+//     into a STAGES-deep shared-memory ring guarded by full/empty mbarriers;
+//   * MMA warp: one elected thread issues 4 tcgen05.mma.kind::f8f6f4 (K = 32 each) per 128-deep
+//     K-block into one of two TMEM accumulators (128 lanes x BN FP32 columns each), a fresh
+//     accumulator per K-block, then tcgen05.commit frees the smem stage and publishes the TMEM
+//     buffer;
+//   * epilogue warps (BN/32 of them; warp w owns TMEM lanes 32*(w%4).. and 128 columns
+//     starting at 128*(w/4)): tcgen05.ld the K-block's partial, scale it by sA·sB and add it into
+//     128 FP32 registers per thread with packed fma.rn.f32x2; release the TMEM buffer right after
+//     the loads so the tensor core runs ahead by one K-block;
+//   * after the last K-block of a tile: round to BF16 (or keep FP32), write 32x64 (32x32 for FP32)
+//     boxes into a 128-byte-swizzled staging buffer and TMA-store them (tails clipped by TMA);
+//     rows that must stay untouched (masked tail, contiguous padding) are stored with predicated
+//     plain stores instead;
+//   * split-K: each split writes its FP32 partial tile to a workspace; the last split to arrive
+//     (per-tile counter) sums all partials in split order 0..S-1 — deterministic — and stores.
+//
+// Tiles: BM = 128 rows (tensor-core M), BN in {128, 256} columns, BK = 128 (one scale block).
+// Every pipeline wait is bounded (see mbar_wait); on a timeout the kernel records
+// DG_DEV_TIMEOUT, stops issuing, drains its own in-flight copies and MMAs, frees TMEM, returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "dg_ptx.cuh"
+
+namespace dg {
+
+enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+
+constexpr int kStatusBadGroup = 0x1;
+constexpr int kStatusBadMaskedM = 0x2;
+
+struct GemmParams {
+  int M;             // dense: M; contiguous: M_total; masked: M_max (rows per group)
+  int N, K, G;
+  int nkb;           // ceil(K / 128): K-blocks (= scale blocks along K)
+  int nnb;           // ceil(N / 128): scale blocks along N
+  int ldsa;          // row stride of the MN-major A scales (M or M_max rounded up to 4)
+  int num_m_blocks;  // ceil(M / 128)
+  int num_n_blocks;  // ceil(N / BN)
+  int num_splits;    // split-K factor
+  int kb_per_split;  // K-blocks per split (the last split may get fewer)
+  int num_tiles;     // dense/contiguous: m_blocks * n_blocks * splits; masked: computed on device
+  int raster_m;      // m-blocks per rasterisation group
+  const float* sA;
+  const float* sB;
+  const int32_t* m_indices;
+  const int32_t* masked_m;
+  void* D;           // row-major, row stride N elements (used by predicated stores)
+  float* workspace;  // split-K partial tiles
+  int* counters;     // split-K arrival counter per output tile (zero between calls)
+  int* status;       // device status word
+};
+
+struct Tile {
+  int g;          // group
+  int m_blk;      // 128-row block within the group (contiguous/dense: within A)
+  int n_blk;      // BN-column block
+  int split;      // K split
+  int out_idx;    // index of the output tile (split-K workspace / counters)
+  int a_row;      // first row of the tile in A's 2-D view (also D's)
+  int rows;       // rows of the tile that exist for this group (<= 128)
+  int kb0, kb1;   // K-block range
+  bool skip;      // nothing to compute (all-padding block, bad group)
+};
+
+// ---------------------------------------------------------------------------------------------
+// Tile scheduling. Every role walks the same sequence of linear tile ids (blockIdx.x, then +grid)
+// and decodes them identically, so the roles agree on every tile without talking to each other.
+
+// Clamped valid-row count of masked group g.
+__device__ __forceinline__ int masked_rows(const GemmParams& p, int g) {
+  int v = __ldg(p.masked_m + g);
+  return v < 0 ? 0 : (v > p.M ? p.M : v);
+}
+
+// Number of (m, n) tiles of the masked problem (warp-cooperative; all lanes return the total).
+__device__ __forceinline__ int masked_total_tiles(const GemmParams& p, int lane, bool report) {
+  int total = 0;
+  for (int g0 = 0; g0 < p.G; g0 += 32) {
+    const int g = g0 + lane;
+    int cnt = 0;
+    if (g < p.G) {
+      const int raw = __ldg(p.masked_m + g);
+      if (report && (raw < 0 || raw > p.M)) atomicOr(p.status, kStatusBadMaskedM);
+      cnt = ((masked_rows(p, g) + 127) / 128) * p.num_n_blocks;
+    }
+    total += __reduce_add_sync(0xffffffffu, cnt);
+  }
+  return total;
+}
+
+// Decodes linear tile id t (warp-cooperative for masked and contiguous modes).
+template <int BN, Mode MODE>
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, int lane) {
+  Tile tile;
+  tile.skip = false;
+  tile.split = t % p.num_splits;
+  const int u = t / p.num_splits;
+  tile.out_idx = u;
+  tile.kb0 = tile.split * p.kb_per_split;
+  tile.kb1 = min(p.nkb, tile.kb0 + p.kb_per_split);
+  if (tile.kb1 <= tile.kb0) tile.skip = true;
+  if constexpr (MODE == kMasked) {
+    // u -> (g, m_blk, n_blk): groups in order, within a group m fastest so the (at most two for
+    // decode-sized groups) m-blocks that share a B tile run side by side.
+    int base = 0;
+    tile.g = -1;
+    for (int g0 = 0; g0 < p.G; g0 += 32) {
+      const int g = g0 + lane;
+      const int rows = g < p.G ? masked_rows(p, g) : 0;
+      const int mb = (rows + 127) / 128;
+      const int cnt = mb * p.num_n_blocks;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int chunk_total = __shfl_sync(0xffffffffu, incl, 31);
+      if (u < base + chunk_total) {
+        const unsigned hit = __ballot_sync(0xffffffffu, base + incl > u);
+        const int L = __ffs(hit) - 1;
+        const int excl = __shfl_sync(0xffffffffu, incl - cnt, L);
+        const int mbL = __shfl_sync(0xffffffffu, mb, L);
+        const int rowsL = __shfl_sync(0xffffffffu, rows, L);
+        const int local = u - base - excl;
+        tile.g = g0 + L;
+        tile.m_blk = local % mbL;
+        tile.n_blk = local / mbL;
+        tile.rows = min(128, rowsL - tile.m_blk * 128);
+        tile.a_row = tile.g * p.M + tile.m_blk * 128;
+        break;
+      }
+      base += chunk_total;
+    }
+    if (tile.g < 0) tile.skip = true;
+  } else {
+    // u -> (m_blk, n_blk) rasterised in groups of raster_m m-blocks: the CTAs running at the same
+    // time cover raster_m m-blocks x (grid / raster_m) n-blocks, so A and B tiles are re-read
+    // from L2 rather than HBM.
+    const int per_group = p.raster_m * p.num_n_blocks;
+    const int grp = u / per_group;
+    const int first_m = grp * p.raster_m;
+    const int gsz = min(p.num_m_blocks - first_m, p.raster_m);
+    const int local = u % per_group;
+    tile.m_blk = first_m + local % gsz;
+    tile.n_blk = local / gsz;
+    tile.a_row = tile.m_blk * 128;
+    tile.rows = min(128, p.M - tile.a_row);
+    tile.g = 0;
+    if constexpr (MODE == kContiguous) {
+      // The block's group is the largest valid index among its rows (padding rows are -1).
+      // Rows with an index outside [-1, G) are flagged and never stored.
+      int mx = -1;
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = tile.a_row + lane * 4 + i;
+        if (r < p.M) {
+          const int idx = __ldg(p.m_indices + r);
+          if (idx >= 0 && idx < p.G) mx = max(mx, idx);
+          bad |= (idx < -1 || idx >= p.G);
+        }
+      }
+      const int g = (int)__reduce_max_sync(0xffffffffu, (unsigned)(mx + 1)) - 1;
+      tile.g = g;
+      if (g < 0) tile.skip = true;               // all padding (or all invalid): nothing to do
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kStatusBadGroup);
+    }
+  }
+  return tile;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Shared-memory plan.
+
+template <int BN, int STAGES>
+struct SmemPlan {
+  static constexpr int kEpiWarps = BN / 32;
+  static constexpr uint32_t kABytes = 128 * 128;
+  static constexpr uint32_t kBBytes = BN * 128;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kStagingPerWarp = 32 * 128;  // one 32-row x 128-byte swizzled box
+  static constexpr uint32_t kStagingOff = STAGES * kStageBytes;
+  static constexpr uint32_t kBarOff = kStagingOff + kEpiWarps * kStagingPerWarp;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 6;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kBytes = kMiscOff + 64;
+  static constexpr uint32_t kDynamicBytes = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kDynamicBytes <= 232448, "shared memory plan exceeds 227 KB");
+};
+
+template <int BN>
+struct Threads {
+  static constexpr int kEpiWarps = BN / 32;
+  static constexpr int kProducerWarp = kEpiWarps;
+  static constexpr int kMmaWarp = kEpiWarps + 1;
+  static constexpr int kCount = 32 * (kEpiWarps + 2);
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// The kernel.
+
+template <int BN, int STAGES, Mode MODE, bool OUT_F32>
+__global__ void __launch_bounds__(Threads<BN>::kCount, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  using Plan = SmemPlan<BN, STAGES>;
+  using T = Threads<BN>;
+  constexpr int kEpiWarps = T::kEpiWarps;
+  constexpr int kEpiThreads = kEpiWarps * 32;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr uint32_t kIdesc = make_idesc_e4m3_f32(128, BN);
+  static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Plan::kBarOff);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* tfull_bar = empty_bar + STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* epi_arrive_bar = tempty_bar + 2;   // split-K: all epilogue warps published a partial
+  uint64_t* epi_release_bar = epi_arrive_bar + 1;  // split-K: the arrival count has been taken
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Plan::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 8);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], kEpiWarps);
+    }
+    mbar_init(epi_arrive_bar, kEpiWarps);
+    mbar_init(epi_release_bar, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == T::kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == T::kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int total_tiles = p.num_tiles;
+  if constexpr (MODE == kMasked) {
+    total_tiles = masked_total_tiles(p, lane, blockIdx.x == 0 && warp == T::kProducerWarp) * p.num_splits;
+  }
+
+  if (warp == T::kProducerWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    uint32_t it = 0;
+    bool alive = true;
+    int issued_phase[STAGES > 0 ? STAGES : 1];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
+    for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
+      const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+      if (tile.skip) continue;
+      const int b_row = tile.g * p.N + tile.n_blk * BN;
+      for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, p.status);
+          if (ok) {
+            uint8_t* sa = smem + s * Plan::kStageBytes;
+            mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
+            tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, l2_policy_evict_last());
+            tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, l2_policy_evict_last());
+            issued_phase[s] = (int)ph;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { alive = false; break; }
+      }
+    }
+    if (!alive && lane == 0) {
+      // Abandoned: let the loads already issued land before the CTA's shared memory goes away.
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued_phase[s] < 0) continue;
+        const uint32_t a = smem_u32(&full_bar[s]);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, (uint32_t)issued_phase[s]) && global_timer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == T::kMmaWarp) {
+    // ------------------------------------------------------------------ tcgen05 MMA issuer
+    uint32_t it = 0, acc_it = 0;
+    bool alive = true;
+    int last_b = -1;
+    uint32_t last_ph = 0;
+    for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
+      const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+      if (tile.skip) continue;
+      for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it, ++acc_it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        const int b = acc_it & 1;
+        const uint32_t aph = (acc_it >> 1) & 1;
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&tempty_bar[b], aph ^ 1, abort_flag, p.status) &&
+               mbar_wait(&full_bar[s], ph, abort_flag, p.status);
+          if (ok) {
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
+            const uint64_t adesc = make_sw128_kmajor_desc(a_addr);
+            const uint64_t bdesc = make_sw128_kmajor_desc(a_addr + Plan::kABytes);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field
+              mma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&empty_bar[s]);
+            mma_commit(&tfull_bar[b]);
+            last_b = b;
+            last_ph = aph;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { alive = false; break; }
+      }
+    }
+    if (!alive && lane == 0 && last_b >= 0) {
+      // Abandoned: wait for the MMAs already issued before TMEM is freed.
+      const uint32_t a = smem_u32(&tfull_bar[last_b]);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(a, last_ph) && global_timer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue warps
+    const int quad = warp % 4;             // TMEM lanes 32*quad .. 32*quad+31
+    const int half = warp / 4;             // columns 128*half .. 128*half+127 of the tile
+    const int row_in_tile = quad * 32 + lane;
+    uint8_t* staging = smem + Plan::kStagingOff + warp * Plan::kStagingPerWarp;
+    const uint32_t staging_addr = smem_u32(staging);
+    uint32_t acc_it = 0, sk_it = 0;
+    bool alive = true;
+    bool store_pending = false;
+    float acc[128];
+
+    for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
+      const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+      if (tile.skip) continue;
+      const int m_local = tile.m_blk * 128 + row_in_tile;   // row within the group
+      const bool row_exists = row_in_tile < tile.rows;
+      const float* sa_ptr = p.sA + (MODE == kMasked ? (size_t)tile.g * p.nkb * p.ldsa : 0) + m_local;
+      const int n_col0 = tile.n_blk * BN + half * 128;       // first column of this warp
+      const int nb = n_col0 / 128;
+      const bool col_exists = n_col0 < p.N;
+      const float* sb_ptr = p.sB + ((size_t)tile.g * p.nnb + (col_exists ? nb : 0)) * p.nkb;
+
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+
+      for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++acc_it) {
+        const int b = acc_it & 1;
+        const uint32_t aph = (acc_it >> 1) & 1;
+        const float sa = row_exists ? __ldg(sa_ptr + (size_t)kb * p.ldsa) : 0.0f;
+        const float sb = col_exists ? __ldg(sb_ptr + kb) : 0.0f;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&tfull_bar[b], aph, abort_flag, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (!ok) { alive = false; break; }
+        tc_fence_after();
+        const float scale = sa * sb;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN + half * 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            ffma2(acc[c * 32 + j], acc[c * 32 + j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]), scale);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[b]);
+      }
+      if (!alive) break;
+
+      // ---------------- split-K: publish the partial, and let the last split reduce
+      if (p.num_splits > 1) {
+        float* ws_tile = p.workspace + (size_t)tile.out_idx * p.num_splits * (128 * BN);
+        float* mine = ws_tile + (size_t)tile.split * (128 * BN);
+        if (row_exists && col_exists) {
+          // layout [column/4][row][4]: a warp's float4 stores are 512 contiguous bytes
+#pragma unroll
+          for (int j = 0; j < 128; j += 4) {
+            const int cq = (half * 128 + j) / 4;
+            __stcg(reinterpret_cast<float4*>(mine + ((size_t)cq * 128 + row_in_tile) * 4),
+                   make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_arrive_bar);
+        int ok = 1;
+        if (warp == 0 && lane == 0) {
+          ok = mbar_wait(epi_arrive_bar, sk_it & 1, abort_flag, p.status);
+          if (ok) {
+            const int prev = atomicAdd(p.counters + tile.out_idx, 1);
+            const int last = (prev == p.num_splits - 1);
+            if (last) p.counters[tile.out_idx] = 0;   // ready for the next call
+            *last_flag = last;
+            mbar_arrive(epi_release_bar);
+          }
+        }
+        if (lane == 0 && ok) ok = mbar_wait(epi_release_bar, sk_it & 1, abort_flag, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        ++sk_it;
+        if (!ok) { alive = false; break; }
+        if (*last_flag == 0) continue;
+        __threadfence();
+        if (row_exists && col_exists) {
+          // total = partial_0 + partial_1 + ... in split order, whichever split arrived last
+#pragma unroll
+          for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+          for (int s = 0; s < p.num_splits; ++s) {
+            const float* src = ws_tile + (size_t)s * (128 * BN);
+#pragma unroll
+            for (int j = 0; j < 128; j += 4) {
+              const int cq = (half * 128 + j) / 4;
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + ((size_t)cq * 128 + row_in_tile) * 4));
+              acc[j] += v.x; acc[j + 1] += v.y; acc[j + 2] += v.z; acc[j + 3] += v.w;
+            }
+          }
+        }
+      }
+
+      // ---------------- output
+      if (!col_exists) continue;
+      bool write_row;
+      if constexpr (MODE == kDense) {
+        write_row = row_exists;
+      } else if constexpr (MODE == kMasked) {
+        write_row = row_exists;   // rows counts only the valid rows of the group
+      } else {
+        write_row = false;
+        if (row_exists) {
+          const int idx = __ldg(p.m_indices + m_local);
+          write_row = (idx == tile.g);
+          if (idx != tile.g && idx != -1) atomicOr(p.status, kStatusBadGroup);
+        }
+      }
+      const int d_row = tile.a_row + row_in_tile;   // row in D's 2-D view
+      if (!__any_sync(0xffffffffu, write_row)) continue;   // no row of this warp is stored
+      const bool use_tma = (MODE == kDense) || __all_sync(0xffffffffu, write_row);
+      if (use_tma) {
+        constexpr int kColsPerBox = OUT_F32 ? 32 : 64;
+#pragma unroll
+        for (int chunk = 0; chunk < 128 / kColsPerBox; ++chunk) {
+          if (n_col0 + chunk * kColsPerBox >= p.N) break;
+          if (store_pending) {
+            if (lane == 0) tma_store_wait_read();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {   // eight 16-byte pieces per 128-byte row
+            uint32_t w0, w1, w2, w3;
+            if constexpr (OUT_F32) {
+              const int c = chunk * 32 + j * 4;
+              w0 = __float_as_uint(acc[c]); w1 = __float_as_uint(acc[c + 1]);
+              w2 = __float_as_uint(acc[c + 2]); w3 = __float_as_uint(acc[c + 3]);
+            } else {
+              const int c = chunk * 64 + j * 8;
+              w0 = pack_bf16x2(acc[c], acc[c + 1]); w1 = pack_bf16x2(acc[c + 2], acc[c + 3]);
+              w2 = pack_bf16x2(acc[c + 4], acc[c + 5]); w3 = pack_bf16x2(acc[c + 6], acc[c + 7]);
+            }
+            const uint32_t phys = (uint32_t)(j ^ (lane & 7));   // 128-byte swizzle
+            st_shared_v4(staging_addr + lane * 128 + phys * 16, w0, w1, w2, w3);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, staging, n_col0 + chunk * kColsPerBox, tile.a_row + quad * 32);
+            tma_store_commit();
+          }
+          store_pending = true;
+          __syncwarp();
+        }
+      } else if (write_row) {
+        // Predicated plain stores: this warp's 32 rows include rows that must stay untouched.
+        if constexpr (OUT_F32) {
+          float* drow = reinterpret_cast<float*>(p.D) + (size_t)d_row * p.N;
+#pragma unroll
+          for (int j = 0; j < 128; j += 4) {
+            if (n_col0 + j < p.N)
+              *reinterpret_cast<float4*>(drow + n_col0 + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+          }
+        } else {
+          uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + (size_t)d_row * p.N;
+#pragma unroll
+          for (int j = 0; j < 128; j += 8) {
+            if (n_col0 + j < p.N) {
+              uint4 v;
+              v.x = pack_bf16x2(acc[j], acc[j + 1]); v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+              v.z = pack_bf16x2(acc[j + 4], acc[j + 5]); v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+              *reinterpret_cast<uint4*>(drow + n_col0 + j) = v;
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == T::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace dg
