@@ -240,7 +240,7 @@ def test_masked_decode_sampled(dg, N, K):
     assert torch.equal(dbits[vt], rne_bf16_bits(D32)[vt])
     rng = np.random.default_rng(N)
     gs, ms = np.nonzero(valid)
-    pick = rng.choice(len(gs), size=3000, replace=False)
+    pick = rng.choice(len(gs), size=3000, replace=len(gs) < 3000)
     gs, ms = gs[pick], ms[pick]
     ns = rng.integers(0, N, len(gs))
     ref = oracle.masked_sampled(a.A, a.sA, b.B, b.sB, gs, ms, ns)
