@@ -125,6 +125,26 @@ dg_status dg_fp8_grouped_masked_f32(const uint8_t* A, const float* sA, const uin
                                     const int32_t* masked_m, float* D, int G, int M_max, int N, int K,
                                     dg_stream_t stream);
 
+/*
+ * Allocation-free dense GEMM: the same computation, arguments and result as dg_fp8_gemm_nt (the
+ * same kernel, tile configuration and accumulation order), for callers that cannot let a library
+ * call cudaMalloc — for example a framework whose caching allocator already owns the device memory,
+ * or a serving loop that must not block on the device synchronisation cudaMalloc/cudaFree may do.
+ * The DeepGEMM pages have no counterpart to this call; it is an addition of this library.
+ *   - It allocates nothing. The split-K partials and arrival counters it may need live in one fixed
+ *     array inside libdg (16 MiB of FP32 partials + 4096 counters, about 16.02 MiB), which every
+ *     device that loads the library holds until the process exits.
+ *   - The first call on each device looks up that array's device address (cudaGetSymbolAddress,
+ *     with the device current) and caches it; make that first call before any stream capture.
+ *   - A shape whose split-K scratch would exceed the array returns DG_ERR_UNSUPPORTED with a message
+ *     naming the sizes (dg_fp8_gemm_nt has no such limit). Shapes that need no split-K use no scratch.
+ *   - Every call on a device shares the array and the array keeps the last call's contents; the call
+ *     clears the counters it uses (an asynchronous memset on `stream`) before its kernel. Calls that
+ *     overlap on the GPU (e.g. on two streams of one device) race on the array and give wrong results.
+ */
+dg_status dg_fp8_gemm_nt_noalloc(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                 uint16_t* D, int M, int N, int K, dg_stream_t stream);
+
 /* x rounded up so that x * elem_bytes is a multiple of 16 bytes (the TMA alignment).
    Source: get_tma_aligned_size, tr.news.hada.io/topic?id=19459, § "Yardımcı fonksiyonlar ve
    ortam değişkenleri". Returns -1 for x < 0 or elem_bytes not in {1, 2, 4, 8, 16}. */

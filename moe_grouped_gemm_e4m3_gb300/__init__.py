@@ -25,7 +25,7 @@ from . import build as _build_mod
 
 __all__ = [
     "DGError", "load", "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_grouped_contiguous",
-    "dg_fp8_grouped_contiguous_f32", "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32",
+    "dg_fp8_grouped_contiguous_f32", "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_fp8_gemm_nt_noalloc",
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms",
     "dg_get_num_sms", "dg_get_device_status", "dg_last_error_string", "dg_query_config",
     "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32",
     "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_get_tma_aligned_size",
     "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms", "dg_get_num_sms", "dg_get_device_status",
-    "dg_last_error_string", "dg_query_config",
+    "dg_last_error_string", "dg_query_config", "dg_fp8_gemm_nt_noalloc",
 )
 
 
@@ -66,7 +66,7 @@ def load(build_if_missing: bool = True):
         raise DGError(DG_ERR_UNSUPPORTED, f"libdg.so not built ({path}); run __graft_entry__.build()")
     lib = ctypes.CDLL(path)
     P, i32 = ctypes.c_void_p, ctypes.c_int
-    for name in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32"):
+    for name in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nt_noalloc"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, i32, i32, i32, P]
     for name in ("dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32"):
@@ -145,6 +145,16 @@ def dg_fp8_gemm_nt(A, sA, B, sB, D, stream=None):
 def dg_fp8_gemm_nt_f32(A, sA, B, sB, D, stream=None):
     """As dg_fp8_gemm_nt, storing the FP32 accumulator."""
     return _dense("dg_fp8_gemm_nt_f32", True, A, sA, B, sB, D, stream)
+
+
+def dg_fp8_gemm_nt_noalloc(A, sA, B, sB, D, stream=None):
+    """As dg_fp8_gemm_nt, without any allocation: for callers that cannot let the library call
+    cudaMalloc (a framework whose caching allocator owns device memory, a serving loop that must not
+    block on cudaMalloc's synchronisation). Split-K scratch comes from a fixed 16 MiB array inside
+    libdg shared by all calls on a device, so calls that overlap on the GPU race; a shape that needs
+    more scratch raises DGError(DG_ERR_UNSUPPORTED). The first call on a device looks up the array's
+    address; make it before any stream capture."""
+    return _dense("dg_fp8_gemm_nt_noalloc", False, A, sA, B, sB, D, stream)
 
 
 def _contig(name, f32, A, sA, B, sB, m_indices, D, stream):

@@ -415,3 +415,127 @@ dg_status dg_query_config(int mode, int M, int N, int K, int G, int out_f32, int
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free dense GEMM.
+//
+// Some callers cannot let a library call cudaMalloc: frameworks whose caching allocator already
+// owns the device memory (a foreign cudaMalloc can fail or fragment their pool), and serving loops
+// that must never block on the implicit device synchronisation cudaMalloc/cudaFree may perform.
+// dg_fp8_gemm_nt_noalloc serves them: the split-K partials and arrival counters live in the
+// fixed array below, which every device that loads libdg holds until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocCounterBytes = 4096 * sizeof(int);                 // 4096 output tiles
+constexpr size_t kNoAllocWorkspaceBytes = size_t(16) << 20;                 // 16 MiB of FP32 partials
+constexpr size_t kNoAllocScratchBytes = kNoAllocCounterBytes + kNoAllocWorkspaceBytes;
+
+}  // namespace
+
+// Layout: [counters: 4096 int][workspace: 16 MiB of float]. Shared by every call on a device.
+static __device__ __align__(256) unsigned char g_dg_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. In host code the array's name is
+// only a host-side stand-in, so its device address is looked up once per device, with that device
+// current, and cached.
+dg_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DG_ERR_UNSUPPORTED, "device ordinal beyond 64");
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dg_noalloc_scratch);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(noalloc scratch)");
+    if (!p) return fail(DG_ERR_CUDA, "cudaGetSymbolAddress returned a null scratch address");
+    g_noalloc_scratch_ptr[dev] = p;
+  }
+  *out = g_noalloc_scratch_ptr[dev];
+  return DG_OK;
+}
+
+}  // namespace
+
+extern "C" dg_status dg_fp8_gemm_nt_noalloc(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                            uint16_t* D, int M, int N, int K, dg_stream_t stream) {
+  t_last_error.clear();
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (M < 0 || N < 0 || K < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
+  if (M == 0 || N == 0) return DG_OK;
+  if (K == 0) return fail(DG_ERR_INVALID_ARG, "K must be positive");
+  if (!A || !sA || !B || !sB || !D) return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
+  if (K % 16 != 0) return fail(DG_ERR_ALIGNMENT, "K must be a multiple of 16 (16-byte rows of E4M3 A and B)");
+  if (N % 8 != 0) return fail(DG_ERR_ALIGNMENT, "N must be a multiple of 8 (16-byte rows of BF16 D)");
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16))
+    return fail(DG_ERR_ALIGNMENT, "A, B and D must be 16-byte aligned");
+  if (!aligned(sA, 4) || !aligned(sB, 4)) return fail(DG_ERR_ALIGNMENT, "sA and sB must be 4-byte aligned");
+  if (M > INT_MAX - 256 || N > INT_MAX - 256 || K > INT_MAX - 256)
+    return fail(DG_ERR_UNSUPPORTED, "a tensor extent exceeds 2^31 - 257");
+
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != DG_OK) return s;
+
+  const Config cfg = choose_config(dg::kDense, M, N, K, 1, effective_sms(*st));
+  const size_t counter_bytes = (size_t)cfg.tiles * sizeof(int);
+  const size_t partial_bytes = (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n * sizeof(float);
+  if (cfg.splits > 1 && (counter_bytes > kNoAllocCounterBytes || partial_bytes > kNoAllocWorkspaceBytes))
+    return fail(DG_ERR_UNSUPPORTED,
+                "dg_fp8_gemm_nt_noalloc: this shape needs " + std::to_string(partial_bytes) + " bytes of split-K "
+                "partials and " + std::to_string(cfg.tiles) + " counters; the fixed scratch holds " +
+                std::to_string(kNoAllocWorkspaceBytes) + " bytes and 4096 counters (use dg_fp8_gemm_nt)");
+
+  dg::LaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  dg::GemmParams& p = a.p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.G = 1;
+  p.nkb = ceil_div(K, 128);
+  p.nnb = ceil_div(N, 128);
+  p.ldsa = dg_get_tma_aligned_size(M, 4);
+  p.num_m_blocks = ceil_div(M, 128);
+  p.num_n_blocks = ceil_div(N, cfg.block_n);
+  p.num_splits = cfg.splits;
+  p.kb_per_split = cfg.kb_per_split;
+  p.num_tiles = cfg.tiles * cfg.splits;
+  p.raster_m = cfg.raster_m;
+  p.sA = sA;
+  p.sB = sB;
+  p.D = D;
+  p.status = st->status;
+  if (cfg.splits > 1) {
+    unsigned char* base = static_cast<unsigned char*>(scratch);
+    p.counters = reinterpret_cast<int*>(base);
+    p.workspace = reinterpret_cast<float*>(base + kNoAllocCounterBytes);
+    // The array keeps whatever the previous call left; the arrival counters must start at zero.
+    cudaError_t e = cudaMemsetAsync(p.counters, 0, counter_bytes, cs);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(noalloc counters)");
+  }
+  if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, 128, 128,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
+    return s;
+  if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, 128,
+                     (uint32_t)cfg.block_n, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
+    return s;
+  if ((s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 64, 32,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, "D")) != DG_OK)
+    return s;
+  a.block_n = cfg.block_n;
+  a.out_f32 = false;
+  a.grid = cfg.grid;
+  a.stream = cs;
+  const cudaError_t e = dg::launch_dense(a);
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return DG_OK;
+}
