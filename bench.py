@@ -42,19 +42,25 @@ SHAPES = [(M, N, K) for M in SWEEP_M for (N, K) in SWEEP_NK]
 WORKLOAD = "dense FP8 E4M3 GEMM sweep, M in {64,128,4096} x (N,K) in {(2112,7168),(24576,1536),(32768,512),(7168,16384),(4096,7168),(7168,2048)}"
 METRIC = "FP8 TFLOPS (2MNK/s) per shape; % of GB300 FP8 dense peak or HBM GB/s"
 L2_FLUSH_BYTES = 256 << 20
-CPU_SAMPLE_PER_SHAPE = 32768
+CPU_SAMPLE_PER_SHAPE = 196608
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=CPU_SAMPLE_PER_SHAPE)
-    return ap.parse_args()
+    ap.add_argument("--shapes", default=None,
+                    help="restrict the sweep to these MxNxK shapes (comma-separated), e.g. for profiling")
+    args = ap.parse_args()
+    if args.shapes:
+        global SHAPES
+        SHAPES = [tuple(int(v) for v in s.lower().split("x")) for s in args.shapes.split(",")]
+    return args
 
 
 def load_peaks():
@@ -317,7 +323,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate (fine-grained scales) -> bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "shapes": len(tensors), "seed": 0, "values": "N(0,1)",
+        "config": {"workload": WORKLOAD if len(tensors) == 18 else f"subset {SHAPES}", "shapes": len(tensors), "seed": 0, "values": "N(0,1)",
                    "quantisation": "E4M3, A 1x128 / B 128x128 FP32 scales, amax/448",
                    "l2": "256 MB write before every GEMM, outside the GEMM's CUDA events",
                    "parallelism": f"replicas x{world}", "wall_ms_per_step": round((t1 - t0) * 1e3 / args.steps, 4)},
@@ -414,7 +420,18 @@ def run_reference(args, rank, world):
     import oracle
     problems = make_inputs()
     threads = oracle.hardware_threads()
-    per_shape = max(64, args.cpu_sample // 8)
+    # Size each step's sample so that the whole --warmup W --steps K run takes about a minute:
+    # calibrate the oracle's rate on a small sample first.
+    calib = cpu_sample_plan(problems, 64, seed=2)
+    t0 = time.perf_counter()
+    cal_flops = 0.0
+    for (M, N, K, a, b, ms, ns) in calib:
+        oracle.gemm_nt_sampled(a.A, a.sA, b.B[0], b.sB[0], ms, ns, threads=threads)
+        cal_flops += 2.0 * K * len(ms)
+    rate = cal_flops / max(time.perf_counter() - t0, 1e-6)
+    flops_per_element = sum(2.0 * K for (M, N, K, a, b) in problems)
+    per_step_budget_s = 60.0 / max(1, args.steps + args.warmup)
+    per_shape = int(min(max(16, rate * per_step_budget_s / flops_per_element), 1 << 20))
     plan = cpu_sample_plan(problems, per_shape, seed=1)
 
     def one_step():

@@ -169,13 +169,13 @@ bool print_configs() {
 
 dg_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapL2promotion promo,
-                    const char* what) {
+                    const char* what, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t elem_strides[2] = {1, 1};
   const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DG_ERR_CUDA, std::string("cuTensorMapEncodeTiled(") + what + ") failed: " + std::to_string((int)r));
   return DG_OK;
@@ -276,11 +276,11 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const float* sA, co
                      (uint32_t)cfg.block_n, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
     return s;
   if (out_f32) {
-    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)N, (uint64_t)rows_total, (uint64_t)N * 4, 32, 32,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D");
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)N, (uint64_t)rows_total, (uint64_t)N * 4, 16, 32,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
   } else {
-    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)rows_total, (uint64_t)N * 2, 64, 32,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D");
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)rows_total, (uint64_t)N * 2, 32, 32,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
   }
   if (s != DG_OK) return s;
 
@@ -528,8 +528,8 @@ extern "C" dg_status dg_fp8_gemm_nt_noalloc(const uint8_t* A, const float* sA, c
   if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, 128,
                      (uint32_t)cfg.block_n, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
     return s;
-  if ((s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 64, 32,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE, "D")) != DG_OK)
+  if ((s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 32, 32,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B)) != DG_OK)
     return s;
   a.block_n = cfg.block_n;
   a.out_f32 = false;

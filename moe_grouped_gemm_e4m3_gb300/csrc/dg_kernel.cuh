@@ -192,30 +192,49 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, int lane
 }
 
 // ---------------------------------------------------------------------------------------------
-// Shared-memory plan.
+// Warp roles, register split and shared-memory plan.
+//
+// Epilogue warps come first, 4 per EPI_COLS-wide column group (one per 32-lane TMEM quadrant);
+// then one more warpgroup holds the producer warp, the MMA warp and two idle warps, so that every
+// warpgroup is whole and can rebalance registers with setmaxnreg.
 
-template <int BN, int STAGES>
+template <int BN, int EPI_COLS>
+struct Roles {
+  static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+  static_assert(EPI_COLS == 64 || EPI_COLS == 128, "EPI_COLS must be 64 or 128");
+  static_assert(BN % EPI_COLS == 0, "EPI_COLS must divide BN");
+  static constexpr int kEpiWarps = 4 * (BN / EPI_COLS);
+  static constexpr int kEpiThreads = kEpiWarps * 32;
+  static constexpr int kProducerWarp = kEpiWarps;
+  static constexpr int kMmaWarp = kEpiWarps + 1;
+  static constexpr int kWarps = kEpiWarps + 4;
+  static constexpr int kThreads = kWarps * 32;
+  // Registers per thread at launch (65536 per SM, allocated for whole 4-warp groups).
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8 > 255 ? 255 : (65536 / kThreads) / 8 * 8;
+  // With more than 8 warps the launch budget is too small for 128 accumulators per epilogue
+  // thread: shift registers from the producer/MMA warpgroup (56) to the epilogue warpgroups.
+  static constexpr bool kRebalance = kThreads > 256;
+  static constexpr int kOtherRegs = 56;
+  static constexpr int kEpiRegs = ((kLaunchRegs * kThreads - kOtherRegs * 128) / kEpiThreads) / 8 * 8;
+  static_assert(!kRebalance || kEpiRegs * kEpiThreads + kOtherRegs * 128 <= kLaunchRegs * kThreads,
+                "register split exceeds the launch budget");
+  static_assert(!kRebalance || kEpiRegs <= 256, "setmaxnreg limit");
+};
+
+template <int BN, int STAGES, int EPI_WARPS, int NBUF>
 struct SmemPlan {
-  static constexpr int kEpiWarps = BN / 32;
   static constexpr uint32_t kABytes = 128 * 128;
   static constexpr uint32_t kBBytes = BN * 128;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kStagingPerWarp = 32 * 128;  // one 32-row x 128-byte swizzled box
+  static constexpr uint32_t kStagingBox = 32 * 64;         // one 32-row x 64-byte swizzled box
+  static constexpr uint32_t kStagingPerWarp = 2 * kStagingBox;  // double-buffered
   static constexpr uint32_t kStagingOff = STAGES * kStageBytes;
-  static constexpr uint32_t kBarOff = kStagingOff + kEpiWarps * kStagingPerWarp;
-  static constexpr uint32_t kNumBars = 2 * STAGES + 6;
+  static constexpr uint32_t kBarOff = kStagingOff + EPI_WARPS * kStagingPerWarp;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 2 * NBUF + 2;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kBytes = kMiscOff + 64;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kDynamicBytes <= 232448, "shared memory plan exceeds 227 KB");
-};
-
-template <int BN>
-struct Threads {
-  static constexpr int kEpiWarps = BN / 32;
-  static constexpr int kProducerWarp = kEpiWarps;
-  static constexpr int kMmaWarp = kEpiWarps + 1;
-  static constexpr int kCount = 32 * (kEpiWarps + 2);
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -228,32 +247,45 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------------------------------------
 // The kernel.
+//
+// TMEM holds a ring of NBUF accumulator buffers of BN FP32 columns (NBUF * BN <= 512), one per
+// K-block in flight. The MMA of K-block kb writes buffer kb % NBUF while the epilogue promotes
+// earlier K-blocks out of the others; an epilogue warp releases a buffer as soon as its last TMEM
+// load has landed, before the FMAs that consume it. The ring's depth is what hides the round trip
+// "MMA done -> commit -> epilogue loads -> release -> next MMA into that buffer".
 
-template <int BN, int STAGES, Mode MODE, bool OUT_F32>
-__global__ void __launch_bounds__(Threads<BN>::kCount, 1)
+template <int BN, int EPI_COLS, int STAGES, int NBUF, Mode MODE, bool OUT_F32>
+__global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
-  using Plan = SmemPlan<BN, STAGES>;
-  using T = Threads<BN>;
-  constexpr int kEpiWarps = T::kEpiWarps;
-  constexpr int kEpiThreads = kEpiWarps * 32;
-  constexpr uint32_t kTmemCols = 2 * BN;
+  using R = Roles<BN, EPI_COLS>;
+  using Plan = SmemPlan<BN, STAGES, R::kEpiWarps, NBUF>;
+  constexpr int kEpiWarps = R::kEpiWarps;
+  constexpr int kChunks = EPI_COLS / 32;   // 32-column TMEM loads per epilogue thread and K-block
+  constexpr uint32_t kTmemCols = NBUF * BN;
+  static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocation: power of two");
   constexpr uint32_t kIdesc = make_idesc_e4m3_f32(128, BN);
-  static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+  static_assert(kChunks % 2 == 0, "TMEM loads go in pairs");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Plan::kBarOff);
   uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* tfull_bar = empty_bar + STAGES;
-  uint64_t* tempty_bar = tfull_bar + 2;
-  uint64_t* epi_arrive_bar = tempty_bar + 2;   // split-K: all epilogue warps published a partial
+  uint64_t* tfull_bar = empty_bar + STAGES;        // [buffer]: the K-block's partial is in TMEM
+  uint64_t* tempty_bar = tfull_bar + NBUF;         // [buffer]: every epilogue warp has loaded it
+  uint64_t* epi_arrive_bar = tempty_bar + NBUF;       // split-K: all epilogue warps published a partial
   uint64_t* epi_release_bar = epi_arrive_bar + 1;  // split-K: the arrival count has been taken
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Plan::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 4);
@@ -267,7 +299,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], kEpiWarps);
     }
@@ -277,12 +309,12 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
     *last_flag = 0;
     fence_barrier_init();
   }
-  if (warp == T::kProducerWarp && lane == 0) {
+  if (warp == R::kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmD);
   }
-  if (warp == T::kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -291,107 +323,115 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  int total_tiles = p.num_tiles;
-  if constexpr (MODE == kMasked) {
-    total_tiles = masked_total_tiles(p, lane, blockIdx.x == 0 && warp == T::kProducerWarp) * p.num_splits;
-  }
-
-  if (warp == T::kProducerWarp) {
-    // ------------------------------------------------------------------ TMA producer
-    uint32_t it = 0;
-    bool alive = true;
-    int issued_phase[STAGES > 0 ? STAGES : 1];
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
-    for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
-      const Tile tile = decode_tile<BN, MODE>(p, t, lane);
-      if (tile.skip) continue;
-      const int b_row = tile.g * p.N + tile.n_blk * BN;
-      for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, p.status);
-          if (ok) {
-            uint8_t* sa = smem + s * Plan::kStageBytes;
-            mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
-            tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, l2_policy_evict_last());
-            tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, l2_policy_evict_last());
-            issued_phase[s] = (int)ph;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) { alive = false; break; }
-      }
+  if (warp >= kEpiWarps) {
+    // ================================================================== producer / MMA warpgroup
+    if constexpr (R::kRebalance) setmaxnreg_dec<R::kOtherRegs>();
+    int total_tiles = p.num_tiles;
+    if constexpr (MODE == kMasked) {
+      if (warp <= R::kMmaWarp)
+        total_tiles = masked_total_tiles(p, lane, blockIdx.x == 0 && warp == R::kProducerWarp) * p.num_splits;
     }
-    if (!alive && lane == 0) {
-      // Abandoned: let the loads already issued land before the CTA's shared memory goes away.
-      for (int s = 0; s < STAGES; ++s) {
-        if (issued_phase[s] < 0) continue;
-        const uint32_t a = smem_u32(&full_bar[s]);
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(a, (uint32_t)issued_phase[s]) && global_timer_ns() - t0 < kWaitLimitNs) {
-        }
-      }
-    }
-  } else if (warp == T::kMmaWarp) {
-    // ------------------------------------------------------------------ tcgen05 MMA issuer
-    uint32_t it = 0, acc_it = 0;
-    bool alive = true;
-    int last_b = -1;
-    uint32_t last_ph = 0;
-    for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
-      const Tile tile = decode_tile<BN, MODE>(p, t, lane);
-      if (tile.skip) continue;
-      for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it, ++acc_it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        const int b = acc_it & 1;
-        const uint32_t aph = (acc_it >> 1) & 1;
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(&tempty_bar[b], aph ^ 1, abort_flag, p.status) &&
-               mbar_wait(&full_bar[s], ph, abort_flag, p.status);
-          if (ok) {
-            tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
-            const uint64_t adesc = make_sw128_kmajor_desc(a_addr);
-            const uint64_t bdesc = make_sw128_kmajor_desc(a_addr + Plan::kABytes);
-            const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+    if (warp == R::kProducerWarp) {
+      // ---------------------------------------------------------------- TMA producer
+      uint32_t it = 0;
+      bool alive = true;
+      int issued_phase[STAGES];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field
-              mma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+      for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
+      const uint64_t policy = l2_policy_evict_last();
+      for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
+        const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+        if (tile.skip) continue;
+        const int b_row = tile.g * p.N + tile.n_blk * BN;
+        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          int ok = 1;
+          if (lane == 0) {
+            ok = mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, p.status);
+            if (ok) {
+              uint8_t* sa = smem + s * Plan::kStageBytes;
+              mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
+              tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
+              tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
+              issued_phase[s] = (int)ph;
             }
-            mma_commit(&empty_bar[s]);
-            mma_commit(&tfull_bar[b]);
-            last_b = b;
-            last_ph = aph;
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) { alive = false; break; }
+        }
+      }
+      if (!alive && lane == 0) {
+        // Abandoned: let the loads already issued land before the CTA's shared memory goes away.
+        for (int s = 0; s < STAGES; ++s) {
+          if (issued_phase[s] < 0) continue;
+          const uint32_t a = smem_u32(&full_bar[s]);
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(a, (uint32_t)issued_phase[s]) && global_timer_ns() - t0 < kWaitLimitNs) {
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) { alive = false; break; }
       }
-    }
-    if (!alive && lane == 0 && last_b >= 0) {
-      // Abandoned: wait for the MMAs already issued before TMEM is freed.
-      const uint32_t a = smem_u32(&tfull_bar[last_b]);
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(a, last_ph) && global_timer_ns() - t0 < kWaitLimitNs) {
+    } else if (warp == R::kMmaWarp) {
+      // ---------------------------------------------------------------- tcgen05 MMA issuer
+      uint32_t it = 0, acc_it = 0;
+      bool alive = true;
+      int last_b = -1;
+      uint32_t last_ph = 0;
+      for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
+        const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+        if (tile.skip) continue;
+        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it, ++acc_it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          const int b = acc_it % NBUF;
+          const uint32_t aph = (acc_it / NBUF) & 1;
+          int ok = 1;
+          if (lane == 0) {
+            ok = mbar_wait(&tempty_bar[b], aph ^ 1, abort_flag, p.status) &&
+                 mbar_wait(&full_bar[s], ph, abort_flag, p.status);
+            if (ok) {
+              tc_fence_after();
+              const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
+              const uint64_t adesc = make_sw128_kmajor_desc(a_addr);
+              const uint64_t bdesc = make_sw128_kmajor_desc(a_addr + Plan::kABytes);
+              const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field
+                mma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+              }
+              mma_commit(&empty_bar[s]);
+              mma_commit(&tfull_bar[b]);
+              last_b = b;
+              last_ph = aph;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) { alive = false; break; }
+        }
+      }
+      if (!alive && lane == 0 && last_b >= 0) {
+        // Abandoned: wait for the MMAs already issued before TMEM is freed.
+        const uint32_t a = smem_u32(&tfull_bar[last_b]);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, last_ph) && global_timer_ns() - t0 < kWaitLimitNs) {
+        }
       }
     }
   } else {
-    // ------------------------------------------------------------------ epilogue warps
-    const int quad = warp % 4;             // TMEM lanes 32*quad .. 32*quad+31
-    const int half = warp / 4;             // columns 128*half .. 128*half+127 of the tile
+    // ================================================================== epilogue warpgroups
+    if constexpr (R::kRebalance) setmaxnreg_inc<R::kEpiRegs>();
+    int total_tiles = p.num_tiles;
+    if constexpr (MODE == kMasked) total_tiles = masked_total_tiles(p, lane, false) * p.num_splits;
+    const int quad = warp % 4;              // TMEM lanes 32*quad .. 32*quad+31
+    const int cgrp = warp / 4;              // columns EPI_COLS*cgrp .. of the tile
     const int row_in_tile = quad * 32 + lane;
     uint8_t* staging = smem + Plan::kStagingOff + warp * Plan::kStagingPerWarp;
     const uint32_t staging_addr = smem_u32(staging);
     uint32_t acc_it = 0, sk_it = 0;
     bool alive = true;
-    bool store_pending = false;
-    float acc[128];
+    uint32_t store_count = 0;   // TMA store boxes issued by this warp
+    float acc[EPI_COLS];        // tile columns EPI_COLS*cgrp + i
 
     for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
       const Tile tile = decode_tile<BN, MODE>(p, t, lane);
@@ -399,40 +439,65 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
       const int m_local = tile.m_blk * 128 + row_in_tile;   // row within the group
       const bool row_exists = row_in_tile < tile.rows;
       const float* sa_ptr = p.sA + (MODE == kMasked ? (size_t)tile.g * p.nkb * p.ldsa : 0) + m_local;
-      const int n_col0 = tile.n_blk * BN + half * 128;       // first column of this warp
-      const int nb = n_col0 / 128;
+      const int n_col0 = tile.n_blk * BN + cgrp * EPI_COLS;  // first column of this warp
       const bool col_exists = n_col0 < p.N;
-      const float* sb_ptr = p.sB + ((size_t)tile.g * p.nnb + (col_exists ? nb : 0)) * p.nkb;
+      const float* sb_ptr = p.sB + ((size_t)tile.g * p.nnb + (col_exists ? n_col0 / 128 : 0)) * p.nkb;
+      // Warps with no row or no column in range only keep the TMEM handshake going.
+      const bool active = col_exists && __any_sync(0xffffffffu, row_exists);
 
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < EPI_COLS; ++i) acc[i] = 0.0f;
+
+      // scales of the first K-block; later ones are fetched one K-block ahead
+      float sa_next = (active && row_exists) ? __ldg(sa_ptr + (size_t)tile.kb0 * p.ldsa) : 0.0f;
+      float sb_next = active ? __ldg(sb_ptr + tile.kb0) : 0.0f;
 
       for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++acc_it) {
-        const int b = acc_it & 1;
-        const uint32_t aph = (acc_it >> 1) & 1;
-        const float sa = row_exists ? __ldg(sa_ptr + (size_t)kb * p.ldsa) : 0.0f;
-        const float sb = col_exists ? __ldg(sb_ptr + kb) : 0.0f;
+        const int b = acc_it % NBUF;
+        const uint32_t aph = (acc_it / NBUF) & 1;
+        const float scale = sa_next * sb_next;
+        if (active && kb + 1 < tile.kb1) {
+          sa_next = row_exists ? __ldg(sa_ptr + (size_t)(kb + 1) * p.ldsa) : 0.0f;
+          sb_next = __ldg(sb_ptr + kb + 1);
+        }
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&tfull_bar[b], aph, abort_flag, p.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();
         if (!ok) { alive = false; break; }
         tc_fence_after();
-        const float scale = sa * sb;
-        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN + half * 128);
+        if (active) {
+          const uint32_t taddr =
+              tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN + cgrp * EPI_COLS);
+          // two 32-column loads in flight per wait; the buffer is released as soon as the last
+          // pair has landed in registers, before its FMAs
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, r);
-          tmem_ld_wait(r);
+          for (int c = 0; c < kChunks; c += 2) {
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, r0);
+            tmem_ld_32x32b_x32(taddr + (c + 1) * 32, r1);
+            tmem_ld_wait(r0);
+            reg_fence(r1);
+            if (c + 2 == kChunks) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty_bar[b]);
+            }
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            ffma2(acc[c * 32 + j], acc[c * 32 + j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]), scale);
+            for (int j = 0; j < 32; j += 2) {
+              ffma2(acc[c * 32 + j], acc[c * 32 + j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), scale);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              ffma2(acc[(c + 1) * 32 + j], acc[(c + 1) * 32 + j + 1], __uint_as_float(r1[j]),
+                    __uint_as_float(r1[j + 1]), scale);
+            }
           }
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[b]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty_bar[b]);
       }
       if (!alive) break;
 
@@ -443,8 +508,8 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
         if (row_exists && col_exists) {
           // layout [column/4][row][4]: a warp's float4 stores are 512 contiguous bytes
 #pragma unroll
-          for (int j = 0; j < 128; j += 4) {
-            const int cq = (half * 128 + j) / 4;
+          for (int j = 0; j < EPI_COLS; j += 4) {
+            const int cq = (cgrp * EPI_COLS + j) / 4;
             __stcg(reinterpret_cast<float4*>(mine + ((size_t)cq * 128 + row_in_tile) * 4),
                    make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
           }
@@ -473,12 +538,12 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
         if (row_exists && col_exists) {
           // total = partial_0 + partial_1 + ... in split order, whichever split arrived last
 #pragma unroll
-          for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-          for (int s = 0; s < p.num_splits; ++s) {
-            const float* src = ws_tile + (size_t)s * (128 * BN);
+          for (int i = 0; i < EPI_COLS; ++i) acc[i] = 0.0f;
+          for (int sp = 0; sp < p.num_splits; ++sp) {
+            const float* src = ws_tile + (size_t)sp * (128 * BN);
 #pragma unroll
-            for (int j = 0; j < 128; j += 4) {
-              const int cq = (half * 128 + j) / 4;
+            for (int j = 0; j < EPI_COLS; j += 4) {
+              const int cq = (cgrp * EPI_COLS + j) / 4;
               const float4 v = __ldcg(reinterpret_cast<const float4*>(src + ((size_t)cq * 128 + row_in_tile) * 4));
               acc[j] += v.x; acc[j + 1] += v.y; acc[j + 2] += v.z; acc[j + 3] += v.w;
             }
@@ -487,7 +552,6 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
       }
 
       // ---------------- output
-      if (!col_exists) continue;
       bool write_row;
       if constexpr (MODE == kDense) {
         write_row = row_exists;
@@ -504,37 +568,43 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
       const int d_row = tile.a_row + row_in_tile;   // row in D's 2-D view
       if (!__any_sync(0xffffffffu, write_row)) continue;   // no row of this warp is stored
       const bool use_tma = (MODE == kDense) || __all_sync(0xffffffffu, write_row);
+      if (!col_exists) continue;
       if (use_tma) {
-        constexpr int kColsPerBox = OUT_F32 ? 32 : 64;
+        // 32-row x 64-byte boxes (32 BF16 or 16 FP32 columns) alternate between two staging
+        // buffers: the TMA engine reads one while the warp fills the other.
+        constexpr int kColsPerBox = OUT_F32 ? 16 : 32;
 #pragma unroll
-        for (int chunk = 0; chunk < 128 / kColsPerBox; ++chunk) {
+        for (int chunk = 0; chunk < EPI_COLS / kColsPerBox; ++chunk) {
           if (n_col0 + chunk * kColsPerBox >= p.N) break;
-          if (store_pending) {
-            if (lane == 0) tma_store_wait_read();
+          const uint32_t sel = store_count & 1;
+          if (store_count >= 2) {
+            if (lane == 0) tma_store_wait_read_1();   // the box that used this buffer has been read
             __syncwarp();
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {   // eight 16-byte pieces per 128-byte row
+          for (int j = 0; j < 4; ++j) {   // four 16-byte pieces per 64-byte row
             uint32_t w0, w1, w2, w3;
             if constexpr (OUT_F32) {
-              const int c = chunk * 32 + j * 4;
+              const int c = chunk * 16 + j * 4;
               w0 = __float_as_uint(acc[c]); w1 = __float_as_uint(acc[c + 1]);
               w2 = __float_as_uint(acc[c + 2]); w3 = __float_as_uint(acc[c + 3]);
             } else {
-              const int c = chunk * 64 + j * 8;
+              const int c = chunk * 32 + j * 8;
               w0 = pack_bf16x2(acc[c], acc[c + 1]); w1 = pack_bf16x2(acc[c + 2], acc[c + 3]);
               w2 = pack_bf16x2(acc[c + 4], acc[c + 5]); w3 = pack_bf16x2(acc[c + 6], acc[c + 7]);
             }
-            const uint32_t phys = (uint32_t)(j ^ (lane & 7));   // 128-byte swizzle
-            st_shared_v4(staging_addr + lane * 128 + phys * 16, w0, w1, w2, w3);
+            // 64-byte swizzle: 16-byte piece j of row r sits at piece j ^ ((r >> 1) & 3)
+            const uint32_t phys = (uint32_t)(j ^ ((lane >> 1) & 3));
+            st_shared_v4(staging_addr + sel * Plan::kStagingBox + lane * 64 + phys * 16, w0, w1, w2, w3);
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmD, staging, n_col0 + chunk * kColsPerBox, tile.a_row + quad * 32);
+            tma_store_2d(&tmD, staging + sel * Plan::kStagingBox, n_col0 + chunk * kColsPerBox,
+                         tile.a_row + quad * 32);
             tma_store_commit();
           }
-          store_pending = true;
+          ++store_count;
           __syncwarp();
         }
       } else if (write_row) {
@@ -542,14 +612,14 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
         if constexpr (OUT_F32) {
           float* drow = reinterpret_cast<float*>(p.D) + (size_t)d_row * p.N;
 #pragma unroll
-          for (int j = 0; j < 128; j += 4) {
+          for (int j = 0; j < EPI_COLS; j += 4) {
             if (n_col0 + j < p.N)
               *reinterpret_cast<float4*>(drow + n_col0 + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
           }
         } else {
           uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + (size_t)d_row * p.N;
 #pragma unroll
-          for (int j = 0; j < 128; j += 8) {
+          for (int j = 0; j < EPI_COLS; j += 8) {
             if (n_col0 + j < p.N) {
               uint4 v;
               v.x = pack_bf16x2(acc[j], acc[j + 1]); v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
@@ -567,7 +637,7 @@ __global__ void __launch_bounds__(Threads<BN>::kCount, 1)
   // ------------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == T::kMmaWarp) {
+  if (warp == R::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }

@@ -21,6 +21,13 @@ struct LaunchArgs {
 // Pipeline depth per tile width (shared-memory plan of the kernel).
 constexpr int stages_for(int block_n) { return block_n == 256 ? 4 : 6; }
 
+// Columns per epilogue warp: 128 for wide tiles (8 epilogue warps), 64 for narrow ones (also 8,
+// so that more warps hide the TMEM-load latency of the promotion).
+constexpr int epi_cols_for(int block_n) { return block_n == 256 ? 128 : 64; }
+
+// TMEM accumulator buffers in the ring: as many as the 512 TMEM columns hold.
+constexpr int tmem_bufs_for(int block_n) { return 512 / block_n; }
+
 cudaError_t launch_dense(const LaunchArgs& a);
 cudaError_t launch_contiguous(const LaunchArgs& a);
 cudaError_t launch_masked(const LaunchArgs& a);
@@ -29,8 +36,11 @@ cudaError_t launch_masked(const LaunchArgs& a);
 template <int BN, Mode MODE, bool OUT_F32>
 cudaError_t launch_instance(const LaunchArgs& a) {
   constexpr int STAGES = stages_for(BN);
-  using Plan = SmemPlan<BN, STAGES>;
-  auto kernel = fp8_gemm_kernel<BN, STAGES, MODE, OUT_F32>;
+  constexpr int EPI_COLS = epi_cols_for(BN);
+  constexpr int NBUF = tmem_bufs_for(BN);
+  using R = Roles<BN, EPI_COLS>;
+  using Plan = SmemPlan<BN, STAGES, R::kEpiWarps, NBUF>;
+  auto kernel = fp8_gemm_kernel<BN, EPI_COLS, STAGES, NBUF, MODE, OUT_F32>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -41,7 +51,7 @@ cudaError_t launch_instance(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  kernel<<<a.grid, Threads<BN>::kCount, Plan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
+  kernel<<<a.grid, R::kThreads, Plan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
   return cudaGetLastError();
 }
 

@@ -58,10 +58,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended in hardware for up to `suspend_ns` waiting for
+// the phase to complete, instead of returning at once: waiting warps then stop taking issue slots
+// from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar_addr, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Time limit of every pipeline wait. No legitimate wait in these kernels comes near it; when it
 // is exceeded the kernel records DG_DEV_TIMEOUT, raises the CTA's abort flag and unwinds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kStatusTimeout = 0x4;
+// Longest hardware suspension of one try_wait inside mbar_wait (the time limit is still checked
+// between suspensions).
+constexpr uint32_t kSuspendHintNs = 1000000u;
 
 // Waits until the phase with the given parity of `bar` has completed. Returns false (and sets
 // *abort) if the CTA's abort flag is raised or the time limit passes; the caller then unwinds.
@@ -71,7 +89,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait_suspend(a, parity, kSuspendHintNs)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       atomicOr(status, kStatusTimeout);
@@ -113,6 +131,11 @@ __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk
 // Waits until every committed store group has finished reading its shared-memory source.
 __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until at most one committed store group is still reading its shared-memory source.
+__device__ __forceinline__ void tma_store_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // Waits until every committed store group is complete (written to global memory).
@@ -224,8 +247,36 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// Ties 32 registers to this point of the instruction stream (no instruction is emitted): no use
+// of them can be scheduled before an earlier volatile asm such as tmem_ld_wait.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // Packed FP32x2 arithmetic (sm_100+): one instruction, two lanes of FP32 fused multiply-add.
+
+// Two FP32 values packed in one 64-bit register pair (low = first).
+__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(lo), "r"(hi));
+  return v;
+}
+
+__device__ __forceinline__ float f32x2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f32x2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
+// acc += a * s on both lanes of packed FP32 pairs (one fma.rn.f32x2; IEEE fused, round to nearest).
+__device__ __forceinline__ void ffma2_acc(uint64_t& acc, uint64_t a, uint64_t s) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(s));
+}
 
 __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float s) {
   uint64_t acc, av, sv;
