@@ -343,23 +343,23 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         const Tile tile = decode_tile<BN, MODE>(p, t, lane);
         if (tile.skip) continue;
         const int b_row = tile.g * p.N + tile.n_blk * BN;
-        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          int ok = 1;
-          if (lane == 0) {
+        // Lane 0 runs the tile's K loop on its own (no warp-wide step per K-block).
+        int ok = 1;
+        if (lane == 0) {
+          for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1;
             ok = mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, p.status);
-            if (ok) {
-              uint8_t* sa = smem + s * Plan::kStageBytes;
-              mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
-              tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
-              tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
-              issued_phase[s] = (int)ph;
-            }
+            if (!ok) break;
+            uint8_t* sa = smem + s * Plan::kStageBytes;
+            mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
+            tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
+            tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
+            issued_phase[s] = (int)ph;
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) { alive = false; break; }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { alive = false; break; }
       }
       if (!alive && lane == 0) {
         // Abandoned: let the loads already issued land before the CTA's shared memory goes away.
@@ -380,35 +380,35 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
         const Tile tile = decode_tile<BN, MODE>(p, t, lane);
         if (tile.skip) continue;
-        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it, ++acc_it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          const int b = acc_it % NBUF;
-          const uint32_t aph = (acc_it / NBUF) & 1;
-          int ok = 1;
-          if (lane == 0) {
+        // Lane 0 runs the tile's K loop on its own (no warp-wide step per K-block).
+        int ok = 1;
+        if (lane == 0) {
+          for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it, ++acc_it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1;
+            const int b = acc_it % NBUF;
+            const uint32_t aph = (acc_it / NBUF) & 1;
             ok = mbar_wait(&tempty_bar[b], aph ^ 1, abort_flag, p.status) &&
                  mbar_wait(&full_bar[s], ph, abort_flag, p.status);
-            if (ok) {
-              tc_fence_after();
-              const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
-              const uint64_t adesc = make_sw128_kmajor_desc(a_addr);
-              const uint64_t bdesc = make_sw128_kmajor_desc(a_addr + Plan::kABytes);
-              const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
+            const uint64_t adesc = make_sw128_kmajor_desc(a_addr);
+            const uint64_t bdesc = make_sw128_kmajor_desc(a_addr + Plan::kABytes);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field
-                mma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
-              }
-              mma_commit(&empty_bar[s]);
-              mma_commit(&tfull_bar[b]);
-              last_b = b;
-              last_ph = aph;
+            for (int k = 0; k < 4; ++k) {
+              // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field
+              mma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
             }
+            mma_commit(&empty_bar[s]);
+            mma_commit(&tfull_bar[b]);
+            last_b = b;
+            last_ph = aph;
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) { alive = false; break; }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { alive = false; break; }
       }
       if (!alive && lane == 0 && last_b >= 0) {
         // Abandoned: wait for the MMAs already issued before TMEM is freed.
@@ -431,7 +431,10 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     uint32_t acc_it = 0, sk_it = 0;
     bool alive = true;
     uint32_t store_count = 0;   // TMA store boxes issued by this warp
-    float acc[EPI_COLS];        // tile columns EPI_COLS*cgrp + i
+    // Tile columns EPI_COLS*cgrp + i, as FP32 pairs so that each promotion step is one packed
+    // fma (__ffma2_rn: two IEEE round-to-nearest FMAs in one instruction).
+    float2 acc2[EPI_COLS / 2];
+    float* const acc = reinterpret_cast<float*>(acc2);
 
     for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
       const Tile tile = decode_tile<BN, MODE>(p, t, lane);
@@ -460,11 +463,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           sa_next = row_exists ? __ldg(sa_ptr + (size_t)(kb + 1) * p.ldsa) : 0.0f;
           sb_next = __ldg(sb_ptr + kb + 1);
         }
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&tfull_bar[b], aph, abort_flag, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        __syncwarp();
-        if (!ok) { alive = false; break; }
+        // All 32 lanes wait together: one warp-wide instruction stream, uniform by construction
+        // (every lane sees the same barrier phase, timer value and abort flag).
+        if (!mbar_wait(&tfull_bar[b], aph, abort_flag, p.status)) { alive = false; break; }
         tc_fence_after();
         if (active) {
           const uint32_t taddr =
@@ -483,14 +484,16 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&tempty_bar[b]);
             }
+            const float2 scale2 = make_float2(scale, scale);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              ffma2(acc[c * 32 + j], acc[c * 32 + j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), scale);
+            for (int j = 0; j < 16; ++j) {
+              acc2[c * 16 + j] = __ffma2_rn(make_float2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1])),
+                                            scale2, acc2[c * 16 + j]);
             }
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              ffma2(acc[(c + 1) * 32 + j], acc[(c + 1) * 32 + j + 1], __uint_as_float(r1[j]),
-                    __uint_as_float(r1[j + 1]), scale);
+            for (int j = 0; j < 16; ++j) {
+              acc2[(c + 1) * 16 + j] = __ffma2_rn(make_float2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1])),
+                                                  scale2, acc2[(c + 1) * 16 + j]);
             }
           }
         } else {
