@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=CPU_SAMPLE_PER_SHAPE)
+    ap.add_argument("--all-configs", action="store_true",
+                    help="time every workload configuration (dense small, sweep, contiguous, masked, stress) "
+                         "and print one JSON line per shape instead of the benchmark line")
     ap.add_argument("--shapes", default=None,
                     help="restrict the sweep to these MxNxK shapes (comma-separated), e.g. for profiling")
     args = ap.parse_args()
@@ -77,6 +80,27 @@ def load_peaks():
 def algorithmic_bytes(M, N, K):
     nkb, nnb = -(-K // 128), -(-N // 128)
     return M * K + N * K + 4 * M * nkb + 4 * nnb * nkb + 2 * M * N
+
+
+def measured_traffic(shape: str):
+    """DRAM bytes (read + write) of one launch of `shape`, from the committed ncu summary, or None
+    when the kernel sources have changed since those counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    h = hashlib.sha256()
+    for src in rec.get("sources", []):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("source_sha256"):
+        return None
+    launch = rec.get("launches", {}).get(shape)
+    if not launch:
+        return None
+    return int(launch["dram_read_bytes"] + launch["dram_write_bytes"])
 
 
 def dist_info():
@@ -289,29 +313,36 @@ def run_ours(args, rank, world, local):
         per_shape.append({"M": M, "N": N, "K": K, "us": round(float(mean_ms[i]) * 1e3, 2), "tflops": round(tflops, 1),
                           "gbs": round(gbs, 1), "bound": bound, "roof_frac": round(frac, 3),
                           "block_n": t["cfg"]["block_n"], "splits": t["cfg"]["splits"]})
-    # dominant kernel: the instantiation (tile width, split-K or not) with the largest share of time
+    # Dominant kernel: the instantiation (tile width, split-K or not) with the largest share of the
+    # step. Its roofline is reported for its longest launch (per-launch figures, as ncu sees them).
     groups = {}
     for i, t in enumerate(tensors):
         key = (t["cfg"]["block_n"], t["cfg"]["splits"] > 1)
-        g = groups.setdefault(key, {"ms": 0.0, "flops": 0.0, "bytes": 0.0, "launches": 0})
+        g = groups.setdefault(key, {"ms": 0.0, "flops": 0.0, "launches": []})
         g["ms"] += float(mean_ms[i])
         g["flops"] += 2.0 * t["M"] * t["N"] * t["K"]
-        g["bytes"] += algorithmic_bytes(t["M"], t["N"], t["K"])
-        g["launches"] += 1
+        g["launches"].append(i)
     dom_key = max(groups, key=lambda k: groups[k]["ms"])
     dom = groups[dom_key]
-    tc_time = dom["flops"] / (fp8_peak * 1e12)
-    hbm_time = dom["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    if tc_time >= hbm_time:
-        achieved = dom["flops"] / (dom["ms"] * 1e-3) / 1e12
+    li = max(dom["launches"], key=lambda i: float(mean_ms[i]))
+    lt = tensors[li]
+    shape = f"{lt['M']}x{lt['N']}x{lt['K']}"
+    l_ms = float(mean_ms[li])
+    l_flops = 2.0 * lt["M"] * lt["N"] * lt["K"]
+    l_bytes = algorithmic_bytes(lt["M"], lt["N"], lt["K"])
+    kname = f"fp8_gemm_kernel<BN={dom_key[0]},{'split-K' if dom_key[1] else 'no split'},dense,bf16>"
+    if l_flops / (fp8_peak * 1e12) >= l_bytes / (peaks["hbm_gbs"] * 1e9):
+        achieved = l_flops / (l_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / fp8_peak, 4)}
     else:
-        achieved = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
+        achieved = l_bytes / (l_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    roof.update({"traffic": None, "kernel": f"fp8_gemm_kernel<BN={dom_key[0]},{'split-K' if dom_key[1] else 'no split'},dense,bf16>",
-                 "launches_per_step": dom["launches"], "share_of_step": round(dom["ms"] / float(mean_ms.sum()), 3),
+    roof.update({"traffic": measured_traffic(shape), "kernel": kname, "launch": shape,
+                 "launch_share_of_step": round(l_ms / float(mean_ms.sum()), 3),
+                 "kernel_share_of_step": round(dom["ms"] / float(mean_ms.sum()), 3),
+                 "kernel_achieved_all_launches": round(dom["flops"] / (dom["ms"] * 1e-3) / 1e12, 1),
                  "peak_source": f"{peaks['source']}: 2 x bf16_tflops (dense FP8 = 2x BF16 nominal)"})
 
     cpu = None
@@ -464,9 +495,88 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_all_configs(args):
+    """One JSON line per shape of every workload configuration: time (CUDA events, mean over reps,
+    L2 flushed before each), TFLOP/s, the binding roof and the fraction of it."""
+    import torch
+    import dg_inputs
+    import moe_grouped_gemm_e4m3_gb300 as dg
+    dg.load()
+    peaks = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    reps = max(3, min(args.steps, 20))
+
+    def timeit(fn):
+        fn()
+        ts = []
+        for r in range(reps):
+            flush.fill_(r & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.mean(ts))
+
+    def report(config, shape, flops, nbytes, ms, extra=None):
+        t_tc, t_hbm = flops / (fp8_peak * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9)
+        bound = "tensor" if t_tc >= t_hbm else "hbm"
+        frac = (flops / (ms * 1e-3) / 1e12 / fp8_peak) if bound == "tensor" else (nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"])
+        line = {"config": config, "shape": shape, "us": round(ms * 1e3, 2), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": bound, "roof_frac": round(frac, 3)}
+        line.update(extra or {})
+        print(json.dumps(line), flush=True)
+
+    def dense(config, M, N, K, dist=dg_inputs.NORMAL, outliers=0.0):
+        a = dg_inputs.make_a(M, K, seed=0, dist=dist, outlier_frac=outliers)
+        b = dg_inputs.make_b(1, N, K, seed=0, dist=dist)
+        A, sA, B, sB = dev(a.A), dev(a.sA), dev(b.B[0]), dev(b.sB[0])
+        D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        ms = timeit(lambda: dg.dg_fp8_gemm_nt(A, sA, B, sB, D))
+        report(config, f"{M}x{N}x{K}", 2.0 * M * N * K, algorithmic_bytes(M, N, K), ms, {"cfg": dg.dg_query_config(0, M, N, K)})
+
+    dense("1 dense small", 128, 512, 1024)
+    for (M, N, K) in [(M, N, K) for M in SWEEP_M for (N, K) in SWEEP_NK]:
+        dense("2 dense sweep", M, N, K)
+    for G in (4, 8):
+        for (N, K) in ((4096, 7168), (7168, 2048)):
+            M = G * 8192
+            a = dg_inputs.make_a(M, K, seed=0)
+            b = dg_inputs.make_b(G, N, K, seed=0)
+            idx = dev(np.repeat(np.arange(G, dtype=np.int32), 8192))
+            A, sA, B, sB = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB)
+            D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            ms = timeit(lambda: dg.dg_fp8_grouped_contiguous(A, sA, B, sB, idx, D))
+            nkb, nnb = -(-K // 128), -(-N // 128)
+            nbytes = M * K + G * N * K + 4 * M * nkb + 4 * G * nnb * nkb + 2 * M * N
+            report("3 contiguous", f"G={G} M={M} N={N} K={K}", 2.0 * M * N * K, nbytes, ms)
+            del A, B, D
+    for (N, K) in ((4096, 7168), (7168, 2048)):
+        G, M_max = 16, 256
+        mm = dg_inputs.make_masked_m(G, M_max, seed=0)
+        a = dg_inputs.make_masked_a(G, M_max, K, seed=0)
+        b = dg_inputs.make_b(G, N, K, seed=0)
+        A, sA, B, sB, MM = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(mm)
+        D = torch.empty(G, M_max, N, dtype=torch.bfloat16, device="cuda")
+        ms = timeit(lambda: dg.dg_fp8_grouped_masked(A, sA, B, sB, MM, D))
+        valid = int(mm.sum())
+        nkb, nnb = -(-K // 128), -(-N // 128)
+        active = int((mm > 0).sum())
+        nbytes = valid * K + active * N * K + 4 * valid * nkb + 4 * G * nnb * nkb + 2 * valid * N
+        report("4 masked", f"G=16 M_max=256 sum(masked_m)={valid} N={N} K={K}", 2.0 * valid * N * K, nbytes, ms)
+    for (M, N, K) in ((4096, 2112, 7168), (4096, 576, 7168), (4096, 7168, 32768)):
+        dense("5 stress (Student-t, outliers)", M, N, K, dist=dg_inputs.STUDENT_T3, outliers=0.01)
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_info()
+    if args.all_configs:
+        run_all_configs(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

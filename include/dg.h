@@ -132,7 +132,7 @@ dg_status dg_fp8_grouped_masked_f32(const uint8_t* A, const float* sA, const uin
  * or a serving loop that must not block on the device synchronisation cudaMalloc/cudaFree may do.
  * The DeepGEMM pages have no counterpart to this call; it is an addition of this library.
  *   - It allocates nothing. The split-K partials and arrival counters it may need live in one fixed
- *     array inside libdg (16 MiB of FP32 partials + 4096 counters, about 16.02 MiB), which every
+ *     array inside libdg (20 MiB of FP32 partials + 4096 counters, about 20.02 MiB), which every
  *     device that loads the library holds until the process exits.
  *   - The first call on each device looks up that array's device address (cudaGetSymbolAddress,
  *     with the device current) and caches it; make that first call before any stream capture.

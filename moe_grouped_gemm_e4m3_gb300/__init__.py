@@ -150,7 +150,7 @@ def dg_fp8_gemm_nt_f32(A, sA, B, sB, D, stream=None):
 def dg_fp8_gemm_nt_noalloc(A, sA, B, sB, D, stream=None):
     """As dg_fp8_gemm_nt, without any allocation: for callers that cannot let the library call
     cudaMalloc (a framework whose caching allocator owns device memory, a serving loop that must not
-    block on cudaMalloc's synchronisation). Split-K scratch comes from a fixed 16 MiB array inside
+    block on cudaMalloc's synchronisation). Split-K scratch comes from a fixed 20 MiB array inside
     libdg shared by all calls on a device, so calls that overlap on the GPU race; a shape that needs
     more scratch raises DGError(DG_ERR_UNSUPPORTED). The first call on a device looks up the array's
     address; make it before any stream capture."""

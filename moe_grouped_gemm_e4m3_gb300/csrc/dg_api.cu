@@ -126,29 +126,71 @@ struct Config {
 };
 
 Config choose_config(int mode, int rows, int N, int K, int G, int num_sms) {
+  // Cost model calibrated on GB300 (sm_103a), times in microseconds per CTA:
+  //  * compute: one K-block (BM=128, BK=128) costs ~0.55 (BN=256) or ~0.50 (BN=128: an N=128 MMA
+  //    takes as long as an N=256 one, for half the work);
+  //  * memory: a CTA streams ~48 GB/s when its operands come from HBM; operands shared by other
+  //    tiles in flight (A across n-blocks, B across m-blocks) come from L2 and cost no HBM time;
+  //  * split-K: the last split reads every partial tile back, ~0.6 (BN=128) / ~1.0 (BN=256) per split;
+  //  * a tile's prologue/epilogue: ~1.5.
+  // Split-K is considered only while all units fit in one wave (more waves never shorten the
+  // critical path). The HBM time of the operands bounds the estimate from below.
+  constexpr double kTileUs = 1.5, kCtaGBs = 48.0, kHbmGBs = 6000.0;
   Config c{};
   const int nkb = ceil_div(K, 128);
+  const int rows_total = rows * (mode == dg::kMasked ? G : 1);
   const int m_blocks = ceil_div(rows, 128) * (mode == dg::kMasked ? G : 1);
+  const double bytes = (double)rows_total * K + (double)(mode == dg::kDense ? 1 : G) * N * K + 2.0 * rows_total * N;
   int bn = N > 128 ? 256 : 128;
-  int tiles = m_blocks * ceil_div(N, bn);
-  if (bn == 256 && tiles < num_sms) {  // too few wide tiles to fill the GPU: use narrow ones
-    bn = 128;
-    tiles = m_blocks * ceil_div(N, bn);
+  int best_s = 1;
+  double best_t = 1e300;
+  const int max_s = (mode == dg::kMasked) ? 1 : kMaxSplits;
+  for (int cand_bn = 128; cand_bn <= 256; cand_bn += 128) {
+    if (cand_bn == 256 && N <= 128) continue;
+    const int n_blocks = ceil_div(N, cand_bn);
+    const int tiles = m_blocks * n_blocks;
+    const double t_compute = cand_bn == 256 ? 0.55 : 0.50;
+    const double t_red = cand_bn == 256 ? 1.0 : 0.6;
+    for (int s = 1; s <= max_s; ++s) {
+      const int kps = ceil_div(nkb, s);
+      const int se = ceil_div(nkb, kps);
+      if (se != s) continue;
+      const long long units = (long long)tiles * se;
+      if (se > 1 && units > num_sms) break;
+      const long long active = units < num_sms ? units : num_sms;
+      // unique HBM bytes per K-block of one tile: its share of A and of B
+      const double a_kb = (double)(rows < 128 ? rows : 128) * 128.0 / n_blocks;
+      const double b_kb = (double)cand_bn * 128.0 / (m_blocks < 16 ? m_blocks : 16);
+      const double cta_gbs = kCtaGBs < kHbmGBs / active ? kCtaGBs : kHbmGBs / active;
+      const double t_mem = (a_kb + b_kb) / (cta_gbs * 1e3);
+      const double t_kb = t_compute > t_mem ? t_compute : t_mem;
+      const double waves = (double)((units + num_sms - 1) / num_sms);
+      double t = waves * (kps * t_kb + kTileUs) + (se > 1 ? t_red * se : 0.0);
+      const double t_hbm = bytes / (kHbmGBs * 1e3);
+      if (t < t_hbm) t = t_hbm;
+      if (t < best_t - 1e-9) { best_t = t; best_s = se; bn = cand_bn; }
+    }
   }
-  int splits = 1;
-  if (mode != dg::kMasked && tiles < num_sms) {
-    // Few tiles (small M): split K so that every SM streams operands; keep >= 2 K-blocks each.
-    splits = num_sms / tiles;
-    if (splits > kMaxSplits) splits = kMaxSplits;
-    if (splits > nkb / 2) splits = nkb / 2;
-    if (splits < 1) splits = 1;
+  const int tiles = m_blocks * ceil_div(N, bn);
+  // Tuning overrides (environment): DG_BLOCK_N in {128, 256} and DG_SPLITS >= 1 (dense and
+  // contiguous only; a split that would exceed one wave of units is still allowed here).
+  int bn_final = bn, tiles_final = tiles;
+  if (const char* e = std::getenv("DG_BLOCK_N")) {
+    const int v = std::atoi(e);
+    if (v == 128 || v == 256) { bn_final = v; tiles_final = m_blocks * ceil_div(N, v); }
   }
-  c.kb_per_split = ceil_div(nkb, splits);
+  if (mode != dg::kMasked) {
+    if (const char* e = std::getenv("DG_SPLITS")) {
+      const int v = std::atoi(e);
+      if (v >= 1 && v <= kMaxSplits) best_s = v < nkb ? v : nkb;
+    }
+  }
+  c.kb_per_split = ceil_div(nkb, best_s);
   c.splits = ceil_div(nkb, c.kb_per_split);
-  c.block_n = bn;
-  c.stages = dg::stages_for(bn);
-  c.tiles = tiles;
-  const long long units = (long long)tiles * c.splits;
+  c.block_n = bn_final;
+  c.stages = dg::stages_for(bn_final);
+  c.tiles = tiles_final;
+  const long long units = (long long)tiles_final * c.splits;
   c.grid = (int)(units < num_sms ? units : num_sms);
   if (c.grid < 1) c.grid = 1;
   const int mb = ceil_div(rows, 128);
@@ -428,12 +470,13 @@ dg_status dg_query_config(int mode, int M, int N, int K, int G, int out_f32, int
 namespace {
 
 constexpr size_t kNoAllocCounterBytes = 4096 * sizeof(int);                 // 4096 output tiles
-constexpr size_t kNoAllocWorkspaceBytes = size_t(16) << 20;                 // 16 MiB of FP32 partials
+constexpr size_t kNoAllocWorkspaceBytes = size_t(20) << 20;                 // 20 MiB of FP32 partials
 constexpr size_t kNoAllocScratchBytes = kNoAllocCounterBytes + kNoAllocWorkspaceBytes;
 
 }  // namespace
 
-// Layout: [counters: 4096 int][workspace: 16 MiB of float]. Shared by every call on a device.
+// Layout: [counters: 4096 int][workspace: 20 MiB of float]. Shared by every call on a device.
+// Split-K uses at most one wave of 128x256 FP32 partial tiles (128 KiB each): 160 of them fit.
 static __device__ __align__(256) unsigned char g_dg_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {

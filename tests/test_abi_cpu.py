@@ -73,8 +73,10 @@ def test_config_heuristic_on_the_gb300_sm_count():
         big = dg.dg_query_config(0, 4096, 7168, 16384)
         assert big["block_n"] == 256 and big["splits"] == 1 and big["grid"] == 152
         small = dg.dg_query_config(0, 64, 2112, 7168)
-        assert small["block_n"] == 128 and small["splits"] > 1
-        assert small["grid"] <= 152 and small["tiles"] * small["splits"] >= small["grid"]
+        assert small["splits"] > 1                                    # few tiles: split K
+        assert small["tiles"] * small["splits"] <= 152                # one wave of units
+        assert small["grid"] == small["tiles"] * small["splits"]
+        assert dg.dg_query_config(0, 64, 128, 1024)["block_n"] == 128  # N <= 128
         masked = dg.dg_query_config(2, 256, 4096, 7168, G=16)
         assert masked["splits"] == 1
         # the configuration never depends on the output type
