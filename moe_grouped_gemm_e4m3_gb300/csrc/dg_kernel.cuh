@@ -232,7 +232,8 @@ struct SmemPlan {
   static constexpr uint32_t kBarOff = kStagingOff + EPI_WARPS * kStagingPerWarp;
   static constexpr uint32_t kNumBars = 2 * STAGES + 2 * NBUF + 2;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kBytes = kMiscOff + 64;
+  static constexpr uint32_t kStashOff = kMiscOff + 64;                 // per epilogue warp: its tile
+  static constexpr uint32_t kBytes = kStashOff + EPI_WARPS * 64;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kDynamicBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
@@ -425,6 +426,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     if constexpr (MODE == kMasked) total_tiles = masked_total_tiles(p, lane, false) * p.num_splits;
     const int quad = warp % 4;              // TMEM lanes 32*quad .. 32*quad+31
     const int cgrp = warp / 4;              // columns EPI_COLS*cgrp .. of the tile
+    // The tile description is parked in shared memory across the K loop, so that only the loop's
+    // own values occupy registers next to the 128 accumulators and the 64 loaded partials.
+    volatile int* stash = reinterpret_cast<volatile int*>(smem + Plan::kStashOff + warp * 64);
     const int row_in_tile = quad * 32 + lane;
     uint8_t* staging = smem + Plan::kStagingOff + warp * Plan::kStagingPerWarp;
     const uint32_t staging_addr = smem_u32(staging);
@@ -437,8 +441,21 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     float* const acc = reinterpret_cast<float*>(acc2);
 
     for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
-      const Tile tile = decode_tile<BN, MODE>(p, t, lane);
-      if (tile.skip) continue;
+      int kb_begin, kb_end;
+      {
+        const Tile tile0 = decode_tile<BN, MODE>(p, t, lane);
+        if (tile0.skip) continue;
+        if (lane == 0) {
+          stash[0] = tile0.g; stash[1] = tile0.m_blk; stash[2] = tile0.n_blk; stash[3] = tile0.split;
+          stash[4] = tile0.out_idx; stash[5] = tile0.a_row; stash[6] = tile0.rows;
+        }
+        kb_begin = tile0.kb0;
+        kb_end = tile0.kb1;
+      }
+      __syncwarp();
+      Tile tile;
+      tile.g = stash[0]; tile.m_blk = stash[1]; tile.n_blk = stash[2];
+      tile.rows = stash[6];
       const int m_local = tile.m_blk * 128 + row_in_tile;   // row within the group
       const bool row_exists = row_in_tile < tile.rows;
       const float* sa_ptr = p.sA + (MODE == kMasked ? (size_t)tile.g * p.nkb * p.ldsa : 0) + m_local;
@@ -452,14 +469,14 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       for (int i = 0; i < EPI_COLS; ++i) acc[i] = 0.0f;
 
       // scales of the first K-block; later ones are fetched one K-block ahead
-      float sa_next = (active && row_exists) ? __ldg(sa_ptr + (size_t)tile.kb0 * p.ldsa) : 0.0f;
-      float sb_next = active ? __ldg(sb_ptr + tile.kb0) : 0.0f;
+      float sa_next = (active && row_exists) ? __ldg(sa_ptr + (size_t)kb_begin * p.ldsa) : 0.0f;
+      float sb_next = active ? __ldg(sb_ptr + kb_begin) : 0.0f;
 
-      for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++acc_it) {
+      for (int kb = kb_begin; kb < kb_end; ++kb, ++acc_it) {
         const int b = acc_it % NBUF;
         const uint32_t aph = (acc_it / NBUF) & 1;
         const float scale = sa_next * sb_next;
-        if (active && kb + 1 < tile.kb1) {
+        if (active && kb + 1 < kb_end) {
           sa_next = row_exists ? __ldg(sa_ptr + (size_t)(kb + 1) * p.ldsa) : 0.0f;
           sb_next = __ldg(sb_ptr + kb + 1);
         }
@@ -503,6 +520,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         }
       }
       if (!alive) break;
+      // the rest of the tile description, back from shared memory
+      tile.split = stash[3]; tile.out_idx = stash[4]; tile.a_row = stash[5];
 
       // ---------------- split-K: publish the partial, and let the last split reduce
       if (p.num_splits > 1) {
