@@ -50,10 +50,10 @@ def _load():
         lib.dgi_fill.argtypes = [u64, u64, i32, i64, i64, P, i32]
         lib.dgi_outlier_channels.restype = i32
         lib.dgi_outlier_channels.argtypes = [u64, i32, dbl, P]
-        lib.dgi_make_a.argtypes = [u64, u64, i32, i64, i32, i32, P, i32, f32, P, P, i64, i32]
-        lib.dgi_quantize_a.argtypes = [P, i32, i32, P, P, i64, i32]
-        lib.dgi_make_b.argtypes = [u64, u64, i32, i32, i32, i32, P, P, i32]
-        lib.dgi_quantize_b.argtypes = [P, i32, i32, i32, P, P, i32]
+        lib.dgi_make_a.argtypes = [u64, u64, i32, i64, i32, i32, P, i32, f32, P, P, i64, i32, i32]
+        lib.dgi_quantize_a.argtypes = [P, i32, i32, P, P, i64, i32, i32]
+        lib.dgi_make_b.argtypes = [u64, u64, i32, i32, i32, i32, P, P, i32, i32]
+        lib.dgi_quantize_b.argtypes = [P, i32, i32, i32, P, P, i32, i32]
         lib.dgi_make_masked_m.argtypes = [u64, i32, i32, i32, P]
         _lib = lib
     return _lib
@@ -120,42 +120,85 @@ class OperandB:
 
 def make_a(M: int, K: int, seed: int = 0, dist: int = NORMAL, base_row: int = 0,
            outlier_frac: float = 0.0, outlier_scale: float = 64.0, stream: int = 0,
-           threads=None) -> OperandA:
+           threads=None, ue8m0: bool = False) -> OperandA:
+    """ue8m0=True quantises with power-of-two scales (smallest 2^p >= amax/448), the scales that
+    the packed-UE8M0 entry points take (pack them with ``pack_ue8m0_a``)."""
     A = np.empty((M, K), dtype=np.uint8)
     sA = np.empty((ceil_div(K, 128), align4(M)), dtype=np.float32)
     ch = outlier_channels(seed, K, outlier_frac) if outlier_frac > 0 else np.zeros(1, np.int32)
     n_out = len(ch) if outlier_frac > 0 else 0
     _load().dgi_make_a(seed, stream, dist, base_row, M, K, _ptr(ch), n_out, outlier_scale,
-                       _ptr(A), _ptr(sA), sA.shape[1], _threads(threads))
+                       _ptr(A), _ptr(sA), sA.shape[1], 1 if ue8m0 else 0, _threads(threads))
     return OperandA(A, sA)
 
 
-def quantize_a(x: np.ndarray, threads=None) -> OperandA:
+def quantize_a(x: np.ndarray, threads=None, ue8m0: bool = False) -> OperandA:
     x = np.ascontiguousarray(x, dtype=np.float32)
     M, K = x.shape
     A = np.empty((M, K), dtype=np.uint8)
     sA = np.empty((ceil_div(K, 128), align4(M)), dtype=np.float32)
-    _load().dgi_quantize_a(_ptr(x), M, K, _ptr(A), _ptr(sA), sA.shape[1], _threads(threads))
+    _load().dgi_quantize_a(_ptr(x), M, K, _ptr(A), _ptr(sA), sA.shape[1], 1 if ue8m0 else 0,
+                           _threads(threads))
     return OperandA(A, sA)
 
 
 def make_b(G: int, N: int, K: int, seed: int = 0, dist: int = NORMAL, stream: int = 1,
-           threads=None) -> OperandB:
+           threads=None, ue8m0: bool = False) -> OperandB:
     B = np.empty((G, N, K), dtype=np.uint8)
     sB = np.empty((G, ceil_div(N, 128), ceil_div(K, 128)), dtype=np.float32)
-    _load().dgi_make_b(seed, stream, dist, G, N, K, _ptr(B), _ptr(sB), _threads(threads))
+    _load().dgi_make_b(seed, stream, dist, G, N, K, _ptr(B), _ptr(sB), 1 if ue8m0 else 0,
+                       _threads(threads))
     return OperandB(B, sB)
 
 
-def quantize_b(x: np.ndarray, threads=None) -> OperandB:
+def quantize_b(x: np.ndarray, threads=None, ue8m0: bool = False) -> OperandB:
     x = np.ascontiguousarray(x, dtype=np.float32)
     if x.ndim == 2:
         x = x[None]
     G, N, K = x.shape
     B = np.empty((G, N, K), dtype=np.uint8)
     sB = np.empty((G, ceil_div(N, 128), ceil_div(K, 128)), dtype=np.float32)
-    _load().dgi_quantize_b(_ptr(x), G, N, K, _ptr(B), _ptr(sB), _threads(threads))
+    _load().dgi_quantize_b(_ptr(x), G, N, K, _ptr(B), _ptr(sB), 1 if ue8m0 else 0, _threads(threads))
     return OperandB(B, sB)
+
+
+def _e8m0_codes(s: np.ndarray) -> np.ndarray:
+    """E8M0 code of each power-of-two FP32 scale in [2^-127, 2^127] (the exponent field; 2^-127,
+    an FP32 subnormal, has exponent field 0 = code 0)."""
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    bits = s.view(np.uint32)
+    frac = bits & 0x7FFFFF
+    expo = (bits >> 23) & 0xFF
+    ok = (s > 0) & (((expo > 0) & (frac == 0)) | ((expo == 0) & (frac == 0x400000)))
+    if not np.all(ok):
+        raise ValueError("scales must be powers of two in [2^-127, 2^127] to pack as UE8M0")
+    return expo.astype(np.uint32)
+
+
+def _pack4(codes: np.ndarray, axis: int) -> np.ndarray:
+    """Packs codes four at a time along `axis` into int32: byte j of word q = entry 4q+j; the
+    bytes past the end are 127 (the scale 1.0)."""
+    codes = np.moveaxis(codes, axis, -1)
+    n = codes.shape[-1]
+    nq = ceil_div(n, 4)
+    padded = np.full(codes.shape[:-1] + (nq * 4,), 127, np.uint32)
+    padded[..., :n] = codes
+    q = padded.reshape(codes.shape[:-1] + (nq, 4))
+    words = q[..., 0] | (q[..., 1] << 8) | (q[..., 2] << 16) | (q[..., 3] << 24)
+    return np.ascontiguousarray(np.moveaxis(words.astype(np.uint32).view(np.int32), -1, axis))
+
+
+def pack_ue8m0_a(sA: np.ndarray) -> np.ndarray:
+    """A's MN-major FP32 scales [..., nkb, ldsa] (powers of two) -> packed UE8M0
+    [..., ceil(nkb/4), ldsa] int32. Padding columns (m >= M, scale 0) pack as 127."""
+    sA = np.array(sA, dtype=np.float32, copy=True)
+    sA[sA == 0] = 1.0
+    return _pack4(_e8m0_codes(sA), axis=-2)
+
+
+def pack_ue8m0_b(sB: np.ndarray) -> np.ndarray:
+    """B's FP32 scales [..., nnb, nkb] (powers of two) -> packed UE8M0 [..., nnb, ceil(nkb/4)]."""
+    return _pack4(_e8m0_codes(sB), axis=-1)
 
 
 def make_masked_m(G: int, M_max: int, seed: int = 0, force_ends: bool = True) -> np.ndarray:
@@ -164,7 +207,8 @@ def make_masked_m(G: int, M_max: int, seed: int = 0, force_ends: bool = True) ->
     return out
 
 
-def make_masked_a(G: int, M_max: int, K: int, seed: int = 0, dist: int = NORMAL, threads=None) -> OperandA:
+def make_masked_a(G: int, M_max: int, K: int, seed: int = 0, dist: int = NORMAL, threads=None,
+                  ue8m0: bool = False) -> OperandA:
     """A[G,M_max,K] and sA[G][ceil(K/128)][align4(M_max)]: group g is rows [g*M_max, (g+1)*M_max)
     of stream 0, each group quantised with its own MN-major scale block."""
     ldsa = align4(M_max)
@@ -176,7 +220,7 @@ def make_masked_a(G: int, M_max: int, K: int, seed: int = 0, dist: int = NORMAL,
         Ag = np.empty((M_max, K), dtype=np.uint8)
         sAg = np.empty((ceil_div(K, 128), ldsa), dtype=np.float32)
         lib.dgi_make_a(seed, 0, dist, g * M_max, M_max, K, _ptr(ch), 0, 64.0,
-                       _ptr(Ag), _ptr(sAg), ldsa, _threads(threads))
+                       _ptr(Ag), _ptr(sAg), ldsa, 1 if ue8m0 else 0, _threads(threads))
         A[g] = Ag
         sA[g] = sAg
     return OperandA(A, sA)

@@ -17,6 +17,8 @@
  * 1x128 K-group of each A row and one per 128x128 block of B, s = amax/448 (448 is the largest
  * finite E4M3 value), q = E4M3(x/s) rounded to nearest-even with saturation. amax == 0 gives
  * s = 1. Partial groups and blocks at the M/N/K tails take amax over the elements present.
+ * For the packed-UE8M0 input form (the DeepGEMM SM100 kernels take UE8M0 scales) the scale is
+ * instead the smallest power of two >= amax/448, so that it is exactly an E8M0 value.
  *
  * A scales are written MN-major ("the LHS scaling factor must be TMA-aligned and transposed",
  * DeepGEMM README summary, section "GEMM arayuzu ve yerlesim kisitlari"): sA[kb][m] with a row
@@ -166,13 +168,29 @@ int dgi_outlier_channels(uint64_t seed, int K, double frac, int32_t* out) {
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Scale of a group with absolute maximum amax. scale_fmt 0: s = amax/448 (FP32, the DeepSeek-V3
+   rule). scale_fmt 1: the smallest power of two >= amax/448, kept in [2^-127, 2^127] so that it
+   is a UE8M0 (OCP MX E8M0) value; the block then never saturates. amax == 0 gives s = 1.      */
+static float dgi_scale(float amax, int scale_fmt) {
+  if (!(amax > 0.0f)) return 1.0f;
+  float t = amax / 448.0f;
+  if (scale_fmt == 0) return t;
+  int e;
+  float f = frexpf(t, &e);            /* t = f * 2^e, f in [0.5, 1) */
+  int p = (f == 0.5f) ? e - 1 : e;    /* 2^p is the smallest power of two >= t */
+  if (p < -127) p = -127;
+  if (p > 127) p = 127;
+  return ldexpf(1.0f, p);
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* A: rows of x drawn (or given), quantised per 1x128 K-group, scales MN-major.               */
 
 typedef struct {
   uint64_t keys[4]; int dist; int64_t base_row;      /* draw mode */
   const float* x;                                    /* given mode (row-major [M,K]) */
   const uint8_t* is_outlier; float outlier_scale;
-  int M, K, nkb; int64_t ldsa;
+  int M, K, nkb; int64_t ldsa; int scale_fmt;
   uint8_t* A; float* sA;
 } dgi_qa_ctx;
 
@@ -193,7 +211,7 @@ static void dgi_qa_body(void* p, int64_t lo, int64_t hi) {
       int k0 = kb * 128, k1 = k0 + 128 < c->K ? k0 + 128 : c->K;
       float amax = 0.0f;
       for (int k = k0; k < k1; ++k) { float v = fabsf(row[k]); if (v > amax) amax = v; }
-      float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+      float s = dgi_scale(amax, c->scale_fmt);
       c->sA[(int64_t)kb * c->ldsa + m] = s;
       for (int k = k0; k < k1; ++k) c->A[m * (int64_t)c->K + k] = dgi_e4m3_encode(row[k] / s);
     }
@@ -206,11 +224,12 @@ static void dgi_qa_body(void* p, int64_t lo, int64_t hi) {
    and is fully written (padding columns m >= M are set to 0). */
 void dgi_make_a(uint64_t seed, uint64_t stream, int dist, int64_t base_row, int M, int K,
                 const int32_t* outlier_ch, int n_outlier, float outlier_scale,
-                uint8_t* A, float* sA, int64_t ldsa, int threads) {
+                uint8_t* A, float* sA, int64_t ldsa, int scale_fmt, int threads) {
   dgi_qa_ctx c;
   memset(&c, 0, sizeof(c));
   for (int s = 0; s < 4; ++s) c.keys[s] = dgi_key(seed, stream, (uint64_t)s);
   c.dist = dist; c.base_row = base_row; c.M = M; c.K = K; c.nkb = (K + 127) / 128; c.ldsa = ldsa;
+  c.scale_fmt = scale_fmt;
   c.A = A; c.sA = sA; c.outlier_scale = outlier_scale;
   uint8_t* flag = NULL;
   if (n_outlier > 0) {
@@ -225,10 +244,12 @@ void dgi_make_a(uint64_t seed, uint64_t stream, int dist, int64_t base_row, int 
 }
 
 /* Quantises a given row-major float32 x[M,K] the same way. */
-void dgi_quantize_a(const float* x, int M, int K, uint8_t* A, float* sA, int64_t ldsa, int threads) {
+void dgi_quantize_a(const float* x, int M, int K, uint8_t* A, float* sA, int64_t ldsa, int scale_fmt,
+                    int threads) {
   dgi_qa_ctx c;
   memset(&c, 0, sizeof(c));
   c.x = x; c.M = M; c.K = K; c.nkb = (K + 127) / 128; c.ldsa = ldsa; c.A = A; c.sA = sA;
+  c.scale_fmt = scale_fmt;
   for (int kb = 0; kb < c.nkb; ++kb)
     for (int64_t m = M; m < ldsa; ++m) sA[(int64_t)kb * ldsa + m] = 0.0f;
   dgi_parallel(dgi_qa_body, &c, M, threads);
@@ -240,7 +261,7 @@ void dgi_quantize_a(const float* x, int M, int K, uint8_t* A, float* sA, int64_t
 typedef struct {
   uint64_t keys[4]; int dist;
   const float* x;
-  int G, N, K, nnb, nkb;
+  int G, N, K, nnb, nkb, scale_fmt;
   uint8_t* B; float* sB;
 } dgi_qb_ctx;
 
@@ -265,7 +286,7 @@ static void dgi_qb_body(void* p, int64_t lo, int64_t hi) {
       float amax = 0.0f;
       for (int r = 0; r < rows; ++r)
         for (int k = k0; k < k1; ++k) { float v = fabsf(strip[(int64_t)r * c->K + k]); if (v > amax) amax = v; }
-      float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+      float s = dgi_scale(amax, c->scale_fmt);
       c->sB[(g * c->nnb + nb) * c->nkb + kb] = s;
       for (int r = 0; r < rows; ++r)
         for (int k = k0; k < k1; ++k)
@@ -277,20 +298,23 @@ static void dgi_qb_body(void* p, int64_t lo, int64_t hi) {
 
 /* Draws B[G,N,K] (row-major element counter over the whole tensor) and quantises it. */
 void dgi_make_b(uint64_t seed, uint64_t stream, int dist, int G, int N, int K,
-                uint8_t* B, float* sB, int threads) {
+                uint8_t* B, float* sB, int scale_fmt, int threads) {
   dgi_qb_ctx c;
   memset(&c, 0, sizeof(c));
   for (int s = 0; s < 4; ++s) c.keys[s] = dgi_key(seed, stream, (uint64_t)s);
   c.dist = dist; c.G = G; c.N = N; c.K = K; c.nnb = (N + 127) / 128; c.nkb = (K + 127) / 128;
+  c.scale_fmt = scale_fmt;
   c.B = B; c.sB = sB;
   dgi_parallel(dgi_qb_body, &c, (int64_t)G * c.nnb, threads);
 }
 
 /* Quantises a given row-major float32 x[G,N,K] the same way. */
-void dgi_quantize_b(const float* x, int G, int N, int K, uint8_t* B, float* sB, int threads) {
+void dgi_quantize_b(const float* x, int G, int N, int K, uint8_t* B, float* sB, int scale_fmt,
+                    int threads) {
   dgi_qb_ctx c;
   memset(&c, 0, sizeof(c));
   c.x = x; c.G = G; c.N = N; c.K = K; c.nnb = (N + 127) / 128; c.nkb = (K + 127) / 128;
+  c.scale_fmt = scale_fmt;
   c.B = B; c.sB = sB;
   dgi_parallel(dgi_qb_body, &c, (int64_t)G * c.nnb, threads);
 }

@@ -7,9 +7,9 @@ of the DeepGEMM pages (or which outside definition: OCP E4M3, IEEE rounding, the
 scale granularity) it follows.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against things other than itself:
-the OCP E4M3 table and torch's float8 conversion, torch's float32->bfloat16 rounding, exact
-integer brute force, closed forms, and the plain dequantise-then-matmul definition computed by
-numpy.
+the OCP E4M3 and E8M0 tables and torch's float8 conversions, torch's float32->bfloat16 rounding,
+exact integer brute force, closed forms, a hand-worked packed-UE8M0 example, and the plain
+dequantise-then-matmul definition computed by numpy.
 """
 from __future__ import annotations
 
@@ -54,6 +54,9 @@ def _load():
         lib.dgo_grouped_masked.argtypes = [P, P, i64, P, P, P, i32, i32, i32, i32, P, P, i32]
         lib.dgo_gemm_nt_sampled.argtypes = [P, P, i64, P, P, i32, i32, i32, i64, P, P, P, i32]
         lib.dgo_hardware_threads.restype = i32
+        lib.dgo_ue8m0_decode.restype = ctypes.c_double
+        lib.dgo_ue8m0_decode.argtypes = [ctypes.c_uint8]
+        lib.dgo_ue8m0_unpack.argtypes = [P, i64, i32, i64, i64, P, i64, i64]
         _lib = lib
     return _lib
 
@@ -179,3 +182,42 @@ def masked_sampled(A, sA, B, sB, gs, ms, ns, threads=None) -> np.ndarray:
         sel = np.nonzero(gs == g)[0]
         out[sel] = gemm_nt_sampled(A[g], sA[g], B[g], sB[g], ms[sel], ns[sel], threads)
     return out
+
+
+# ---------------------------------------------------------------------------------------------
+# Packed UE8M0 scales (four OCP E8M0 codes per int32; byte j of word q is K-group 4q+j). The GEMM
+# with such scales is the GEMM above with the unpacked (exact, power-of-two) FP32 scales.
+
+
+def ue8m0_decode(codes) -> np.ndarray:
+    """FP64 value of each E8M0 byte: 2^(e-127), NaN for 0xFF."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.dgo_ue8m0_decode(int(c)) for c in codes.ravel()], dtype=np.float64).reshape(codes.shape)
+
+
+def unpack_ue8m0_a(sA_packed, nkb: int) -> np.ndarray:
+    """A's MN-major packed scales [..., ceil(nkb/4), ldsa] int32 -> FP32 [..., nkb, ldsa]."""
+    p = np.ascontiguousarray(sA_packed, dtype=np.int32)
+    lead, (nkq, ldsa) = p.shape[:-2], p.shape[-2:]
+    assert nkq == (nkb + 3) // 4
+    p2 = p.reshape(-1, nkq, ldsa)
+    out = np.empty((p2.shape[0], nkb, ldsa), np.float32)
+    lib = _load()
+    for g in range(p2.shape[0]):
+        pg = np.ascontiguousarray(p2[g])
+        og = np.empty((nkb, ldsa), np.float32)
+        lib.dgo_ue8m0_unpack(_p(pg), ldsa, nkb, 1, ldsa, _p(og), 1, ldsa)
+        out[g] = og
+    return out.reshape(*lead, nkb, ldsa)
+
+
+def unpack_ue8m0_b(sB_packed, nkb: int) -> np.ndarray:
+    """B's packed scales [..., nnb, ceil(nkb/4)] int32 -> FP32 [..., nnb, nkb]."""
+    p = np.ascontiguousarray(sB_packed, dtype=np.int32)
+    lead, (nnb, nkq) = p.shape[:-2], p.shape[-2:]
+    assert nkq == (nkb + 3) // 4
+    flat = np.ascontiguousarray(p.reshape(-1, nkq))
+    out = np.empty((flat.shape[0], nkb), np.float32)
+    _load().dgo_ue8m0_unpack(_p(flat), flat.shape[0], nkb, nkq, 1, _p(out), nkb, 1)
+    return out.reshape(*lead, nnb, nkb)

@@ -31,6 +31,12 @@
 //     bits; exponent field 15 with mantissa 7 is NaN; no infinities; largest finite value 448).
 //   * BF16 output rounding: IEEE round-to-nearest-even, taken directly from the FP64 value (no
 //     intermediate FP32 rounding).
+//   * Packed UE8M0 scales (the Blackwell input form): the SM100 implementation takes its scaling
+//     factors as UE8M0 values, four of them packed into one 32-bit integer (same page, § "GEMM
+//     arayüzü ve yerleşim kısıtları"). UE8M0 is the OCP Microscaling (MX) v1.0 E8M0 format
+//     (§ 5.4.1): eight exponent bits with bias 127, no sign, no mantissa, 0xFF is NaN; the value of
+//     code e is 2^(e-127). Byte j (bits 8j..8j+7) of packed word q holds K-group 4q+j. Such scales
+//     are powers of two, so unpacking them into FP32 is exact and the GEMM is the one above.
 //
 // Exactness: every product of two E4M3 values has at most 8 significant bits and lies in
 // [2^-18, 448^2]; 128 of them sum exactly in FP64 (53 bits). (sA·sB) of two FP32 values is exact
@@ -86,6 +92,12 @@ uint16_t bf16_rne(double x) {
 }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// OCP MX E8M0 decode, written from the format definition.
+double ue8m0_value(uint8_t code) {
+  if (code == 0xFF) return std::nan("");
+  return std::ldexp(1.0, (int)code - 127);
+}
 
 // One output element: Σ_kb sA[m,kb]·sB[n/128,kb]·P_kb with P_kb the exact FP64 partial.
 //   a_row : the K bytes of row m of A          sA_m : pointer to sA[0][m], stride ldsa per kb
@@ -208,6 +220,24 @@ void dgo_gemm_nt_sampled(const uint8_t* A, const float* sA, int64_t ldsa, const 
     const int64_t m = ms[i], n = ns[i];
     out[i] = element(A + m * K, sA + m, ldsa, B + n * K, sB + (n / 128) * nkb, K);
   });
+}
+
+double dgo_ue8m0_decode(uint8_t code) { return ue8m0_value(code); }
+
+// Unpacks UE8M0 scales, four per 32-bit word, into FP32 (exact: every value is a power of two in
+// [2^-127, 2^127], or NaN). Item i's scale of K-group kb is byte (kb % 4) of
+// packed[(kb / 4) * stride_quad + i * stride_item]; it is written to out[i * out_item + kb * out_kb].
+//   A's MN-major scales [ceil(nkb/4)][ldsa]:  stride_item = 1,    stride_quad = ldsa
+//   B's scales [nnb][ceil(nkb/4)] per group:  stride_item = nkq,  stride_quad = 1
+void dgo_ue8m0_unpack(const int32_t* packed, int64_t n_items, int nkb, int64_t stride_item,
+                      int64_t stride_quad, float* out, int64_t out_item, int64_t out_kb) {
+  for (int64_t i = 0; i < n_items; ++i) {
+    for (int kb = 0; kb < nkb; ++kb) {
+      const uint32_t word = (uint32_t)packed[(int64_t)(kb / 4) * stride_quad + i * stride_item];
+      const uint8_t code = (uint8_t)((word >> (8 * (kb % 4))) & 0xFFu);
+      out[i * out_item + (int64_t)kb * out_kb] = (float)ue8m0_value(code);
+    }
+  }
 }
 
 // Number of hardware threads of this host (the oracle's default parallelism).

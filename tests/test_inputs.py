@@ -84,3 +84,39 @@ def test_outliers_and_masked_m():
     assert mm[0] == 0 and mm[-1] == 256 and np.all((mm >= 0) & (mm <= 256))
     idx = dg_inputs.contiguous_m_indices([3, 0, 130], pad_to=128)
     assert len(idx) == 128 + 256 and (idx == -1).sum() == 125 + 126
+
+
+def test_ue8m0_scales_are_the_smallest_sufficient_powers_of_two():
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((21, 400)) * np.exp(rng.uniform(-20, 20, (21, 1)))).astype(np.float32)
+    x[5, 128:256] = 0
+    qa = dg_inputs.quantize_a(x, ue8m0=True)
+    table = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for kb in range(4):
+        sl = slice(kb * 128, min(400, kb * 128 + 128))
+        t = np.abs(x[:, sl]).max(axis=1) / np.float32(448)
+        s = qa.sA[kb, :21].astype(np.float64)
+        m, _ = np.frexp(s)
+        assert np.all(m == 0.5)                                   # powers of two
+        nz = t > 0
+        assert np.all(s[nz] >= t[nz]) and np.all(s[nz] / 2 < t[nz])
+        assert np.all(s[~nz] == 1.0)
+        assert np.all(np.abs(table[qa.A[:, sl]]) <= 448)
+    qb = dg_inputs.quantize_b(x[None, :, :256], ue8m0=True)
+    m, _ = np.frexp(qb.sB.astype(np.float64))
+    assert np.all(m == 0.5)
+
+
+def test_pack_ue8m0_layout_and_padding():
+    sA = np.array([[1.0, 2.0, 0.0, 0.0], [0.5, 4.0, 0.0, 0.0], [2.0 ** -127, 2.0 ** 127, 0.0, 0.0],
+                   [1.0, 1.0, 0.0, 0.0], [8.0, 0.25, 0.0, 0.0]], np.float32)      # [nkb=5][ldsa=4]
+    p = dg_inputs.pack_ue8m0_a(sA).view(np.uint32)
+    assert p.shape == (2, 4)
+    assert hex(p[0, 0]) == hex(0x7F007E7F) and hex(p[0, 1]) == hex(0x7FFE8180)
+    assert hex(p[1, 0]) == hex(0x7F7F7F82) and hex(p[1, 1]) == hex(0x7F7F7F7D)
+    assert np.all(p[:, 2:] == 0x7F7F7F7F)
+    sB = np.array([[[1.0, 2.0, 4.0, 8.0, 16.0]]], np.float32)                    # [G=1][nnb=1][nkb=5]
+    q = dg_inputs.pack_ue8m0_b(sB).view(np.uint32)
+    assert q.shape == (1, 1, 2) and q[0, 0, 0] == 0x8281807F and q[0, 0, 1] == 0x7F7F7F83
+    with np.testing.assert_raises(ValueError):
+        dg_inputs.pack_ue8m0_b(np.array([[[3.0]]], np.float32))

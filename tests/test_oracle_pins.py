@@ -9,6 +9,10 @@
   random inputs (pins the scale indexing); identity B; scale linearity; a single K-block.
 * Grouped forms: contiguous and masked equal the dense oracle per group, bit for bit, and rows
   outside the valid region stay untouched.
+* Packed UE8M0 scales: the OCP MX E8M0 table (golden file) and torch's float8_e8m0fnu conversion
+  for all 256 codes; a GEMM with packed scales worked by hand (golden file, pins the byte order
+  and both packed layouts); the unpacker against the input generator's independent packer; the
+  dequantise-then-matmul definition with power-of-two scales.
 """
 import math
 import os
@@ -334,3 +338,88 @@ def test_sampled_matches_full():
     ms, ns = rng.integers(0, M, 200), rng.integers(0, N, 200)
     got = oracle.gemm_nt_sampled(a.A, a.sA, b.B[0], b.sB[0], ms, ns, threads=3)
     assert np.array_equal(got, ref64[ms, ns])
+
+
+# ----------------------------------------------------------------------------------------------
+# Packed UE8M0 scales
+
+
+def test_ue8m0_golden_table():
+    with open(os.path.join(GOLDEN, "ue8m0_values.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) >= 10
+    for code_s, val_s in rows:
+        got = float(oracle.ue8m0_decode(np.array([int(code_s, 16)], np.uint8))[0])
+        if val_s == "nan":
+            assert math.isnan(got), code_s
+        else:
+            assert got == float(val_s), code_s
+
+
+def test_ue8m0_all_codes_vs_torch():
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("this torch has no float8_e8m0fnu")
+    ours = oracle.ue8m0_decode(np.arange(256, dtype=np.uint8))
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    assert np.isnan(ours[255]) and np.isnan(ref[255])
+    assert np.array_equal(ours[:255], ref[:255])
+    assert np.all(np.diff(ours[:255]) > 0) and np.all(ours[1:255] == 2 * ours[:254])
+
+
+def _read_packed_example():
+    vals = {}
+    rows_a, rows_b = {}, {}
+    with open(os.path.join(GOLDEN, "ue8m0_packed_example.txt")) as f:
+        for ln in f:
+            if not ln.strip() or ln.startswith("#"):
+                continue
+            key, *rest = ln.split()
+            if key == "A_row_group_values":
+                rows_a[int(rest[0])] = [float(v) for v in rest[1:]]
+            elif key == "B_row_group_values":
+                rows_b[int(rest[0])] = [float(v) for v in rest[1:]]
+            else:
+                vals[key] = rest
+    return vals, rows_a, rows_b
+
+
+def test_ue8m0_packed_worked_example_by_hand():
+    vals, rows_a, rows_b = _read_packed_example()
+    M, N, K = int(vals["M"][0]), int(vals["N"][0]), int(vals["K"][0])
+    nkb = K // 128
+    a_val = np.array([np.repeat(rows_a[m], 128) for m in range(M)], np.float32)
+    b_val = np.array([np.repeat(rows_b[n], 128) for n in range(N)], np.float32)
+    A, B = _e4m3_bytes_of_exact(a_val), _e4m3_bytes_of_exact(b_val)
+    words = lambda key: np.array([int(w, 16) for w in vals[key]], np.uint32).view(np.int32)
+    sA_packed = words("sA_packed").reshape((nkb + 3) // 4, dg_inputs.align4(M))
+    sB_packed = words("sB_packed").reshape(1, (nkb + 3) // 4)
+    sA = oracle.unpack_ue8m0_a(sA_packed, nkb)
+    sB = oracle.unpack_ue8m0_b(sB_packed, nkb)
+    ref64, D = oracle.gemm_nt(A, sA, B, sB, threads=1)
+    assert ref64.ravel().tolist() == [float(v) for v in vals["D64"]]
+    assert D.ravel().tolist() == [int(v, 16) for v in vals["D_bf16"]]
+
+
+@pytest.mark.parametrize("G,M,N,K", [(1, 7, 130, 640), (2, 130, 40, 1024), (3, 1, 257, 200)])
+def test_ue8m0_unpack_inverts_the_generators_packer(G, M, N, K):
+    a = dg_inputs.make_a(M, K, seed=12, ue8m0=True)
+    b = dg_inputs.make_b(G, N, K, seed=12, ue8m0=True)
+    nkb = (K + 127) // 128
+    sA = oracle.unpack_ue8m0_a(dg_inputs.pack_ue8m0_a(a.sA), nkb)
+    sB = oracle.unpack_ue8m0_b(dg_inputs.pack_ue8m0_b(b.sB), nkb)
+    assert np.array_equal(sA[:, :M], a.sA[:, :M])
+    assert np.all(sA[:, M:] == 1.0)                     # padding columns pack as code 127
+    assert np.array_equal(sB, b.sB)
+
+
+@pytest.mark.parametrize("M,N,K,dist", [(40, 300, 896, dg_inputs.NORMAL), (129, 64, 272, dg_inputs.STUDENT_T3)])
+def test_ue8m0_gemm_matches_dequantised_definition(M, N, K, dist):
+    a = dg_inputs.make_a(M, K, seed=13, dist=dist, ue8m0=True)
+    b = dg_inputs.make_b(1, N, K, seed=13, dist=dist, ue8m0=True)
+    nkb = (K + 127) // 128
+    sA = oracle.unpack_ue8m0_a(dg_inputs.pack_ue8m0_a(a.sA), nkb)
+    sB = oracle.unpack_ue8m0_b(dg_inputs.pack_ue8m0_b(b.sB[0]), nkb)
+    ref64, _ = oracle.gemm_nt(a.A, sA, b.B[0], sB, threads=4)
+    want = _numpy_definition(a.A, a.sA, b.B[0], b.sB[0])
+    scale = np.abs(want).max()
+    assert np.abs(ref64 - want).max() <= 1e-13 * scale
