@@ -126,6 +126,42 @@ dg_status dg_fp8_grouped_masked_f32(const uint8_t* A, const float* sA, const uin
                                     dg_stream_t stream);
 
 /*
+ * Packed-UE8M0 variants: the same three GEMMs when every scale is a power of two, given as UE8M0
+ * codes (OCP MX E8M0: value 2^(e-127); 0xFF is NaN) packed four to a 32-bit word, the scale form
+ * the DeepGEMM SM100 kernels take ("DeepGEMM: İnce ölçeklendirmeyle temiz ve verimli FP8 GEMM
+ * çekirdekleri", tr.news.hada.io/topic?id=19459, § "GEMM arayüzü ve yerleşim kısıtları": the
+ * SM100 implementation wants packed UE8M0, four UE8M0 values in one torch.int). The granularity is
+ * unchanged: one scale per 1x128 K-group of each A row and one per 128x128 block of B.
+ *   Packing: byte j (bits 8j..8j+7) of word q holds K-group 4q+j; unused bytes past ceil(K/128)
+ *   are ignored.
+ *   sA: int32, MN-major: sA[(g * ceil(nkb/4) + q) * ldsa + m], ldsa = dg_get_tma_aligned_size(rows, 4)
+ *       (dense and contiguous: g = 0), nkb = ceil(K/128).
+ *   sB: int32, sB[(g * ceil(N/128) + nb) * ceil(nkb/4) + q].
+ * Because such scales are powers of two, the tensor core applies them itself (block-scaled MMA,
+ * tcgen05.mma kind::mxf8f6f4 with scale_vec::1X) and the K loop accumulates in one FP32 TMEM
+ * accumulator: there is no per-128-K promotion on CUDA cores, so the FP32 result can differ from
+ * the FP32-scale calls' in its rounding, not in its value. Every other convention (layouts,
+ * alignment, errors, device status, split-K workspace, the *_f32 variants) is that of the
+ * corresponding FP32-scale call. The tile width is always 256 columns.
+ */
+dg_status dg_fp8_gemm_nt_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                               uint16_t* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_nt_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                   float* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_grouped_contiguous_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                          const int32_t* sB, const int32_t* m_indices, uint16_t* D,
+                                          int M_total, int N, int K, int G, dg_stream_t stream);
+dg_status dg_fp8_grouped_contiguous_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                              const int32_t* sB, const int32_t* m_indices, float* D,
+                                              int M_total, int N, int K, int G, dg_stream_t stream);
+dg_status dg_fp8_grouped_masked_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                      const int32_t* masked_m, uint16_t* D, int G, int M_max, int N, int K,
+                                      dg_stream_t stream);
+dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                          const int32_t* sB, const int32_t* masked_m, float* D, int G, int M_max,
+                                          int N, int K, dg_stream_t stream);
+
+/*
  * Allocation-free dense GEMM: the same computation, arguments and result as dg_fp8_gemm_nt (the
  * same kernel, tile configuration and accumulation order), for callers that cannot let a library
  * call cudaMalloc — for example a framework whose caching allocator already owns the device memory,
@@ -172,6 +208,8 @@ const char* dg_last_error_string(void);
    {block_m, block_n, stages, splits, grid, num_tiles_upper_bound}. Setting the environment
    variable DG_PRINT_CONFIGS=1 prints the same per call on stderr. */
 dg_status dg_query_config(int mode, int M, int N, int K, int G, int out_f32, int* cfg);
+/* The same for the packed-UE8M0 calls. */
+dg_status dg_query_config_ue8m0(int mode, int M, int N, int K, int G, int out_f32, int* cfg);
 
 #ifdef __cplusplus
 }

@@ -10,6 +10,9 @@ The names mirror the C ABI:
 * ``dg_fp8_grouped_contiguous(A, sA, B, sB, m_indices, D)``  M-grouped, contiguous layout
 * ``dg_fp8_grouped_masked(A, sA, B, sB, masked_m, D)``       M-grouped, masked layout
 * ``*_f32`` variants store the FP32 accumulator instead of BF16 (same kernel and order).
+* ``*_ue8m0`` variants take power-of-two scales as packed UE8M0 int32 words (four K-groups per
+  word, byte j = K-group 4q+j): sA int32 [ceil(ceil(K/128)/4), align4(rows)] (masked: leading G),
+  sB int32 [G, ceil(N/128), ceil(ceil(K/128)/4)]. They run the block-scaled tensor-core kernel.
 
 Tensor contract (all CUDA, contiguous): A uint8/float8_e4m3fn [rows, K] (masked: [G, M_max, K]);
 B uint8/float8_e4m3fn [N, K] or [G, N, K]; sA float32 MN-major [ceil(K/128), align4(rows)]
@@ -28,7 +31,9 @@ __all__ = [
     "dg_fp8_grouped_contiguous_f32", "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_fp8_gemm_nt_noalloc",
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms",
     "dg_get_num_sms", "dg_get_device_status", "dg_last_error_string", "dg_query_config",
-    "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
+    "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
+    "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
+    "dg_query_config_ue8m0", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
     "DG_DEV_TIMEOUT",
 ]
@@ -42,6 +47,9 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_get_tma_aligned_size",
     "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms", "dg_get_num_sms", "dg_get_device_status",
     "dg_last_error_string", "dg_query_config", "dg_fp8_gemm_nt_noalloc",
+    "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
+    "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
+    "dg_query_config_ue8m0",
 )
 
 
@@ -66,13 +74,16 @@ def load(build_if_missing: bool = True):
         raise DGError(DG_ERR_UNSUPPORTED, f"libdg.so not built ({path}); run __graft_entry__.build()")
     lib = ctypes.CDLL(path)
     P, i32 = ctypes.c_void_p, ctypes.c_int
-    for name in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nt_noalloc"):
+    for name in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nt_noalloc", "dg_fp8_gemm_nt_ue8m0",
+                 "dg_fp8_gemm_nt_ue8m0_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, i32, i32, i32, P]
-    for name in ("dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32"):
+    for name in ("dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32", "dg_fp8_grouped_contiguous_ue8m0",
+                 "dg_fp8_grouped_contiguous_ue8m0_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
-    for name in ("dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32"):
+    for name in ("dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_fp8_grouped_masked_ue8m0",
+                 "dg_fp8_grouped_masked_ue8m0_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
     lib.dg_get_tma_aligned_size.restype, lib.dg_get_tma_aligned_size.argtypes = i32, [i32, i32]
@@ -82,8 +93,9 @@ def load(build_if_missing: bool = True):
     lib.dg_get_num_sms.restype, lib.dg_get_num_sms.argtypes = i32, []
     lib.dg_get_device_status.restype, lib.dg_get_device_status.argtypes = i32, [ctypes.POINTER(i32), P]
     lib.dg_last_error_string.restype, lib.dg_last_error_string.argtypes = ctypes.c_char_p, []
-    lib.dg_query_config.restype = i32
-    lib.dg_query_config.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
+    for name in ("dg_query_config", "dg_query_config_ue8m0"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i32, [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
     _lib = lib
     return lib
 
@@ -123,6 +135,11 @@ def _f32():
     return (torch.float32,)
 
 
+def _scale_types(name):
+    import torch
+    return (torch.int32,) if "_ue8m0" in name else (torch.float32,)
+
+
 def _d_types(f32: bool):
     import torch
     return (torch.float32,) if f32 else (torch.bfloat16, torch.int16, torch.uint16)
@@ -132,8 +149,8 @@ def _dense(name, f32, A, sA, B, sB, D, stream):
     lib = load()
     M, K = A.shape
     N = B.shape[-2]
-    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
-                              _ptr(sB, "sB", _f32()), _ptr(D, "D", _d_types(f32)), M, N, K, _stream(stream)))
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _scale_types(name)), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", _scale_types(name)), _ptr(D, "D", _d_types(f32)), M, N, K, _stream(stream)))
     return D
 
 
@@ -162,8 +179,8 @@ def _contig(name, f32, A, sA, B, sB, m_indices, D, stream):
     lib = load()
     M, K = A.shape
     G, N = B.shape[0], B.shape[1]
-    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
-                              _ptr(sB, "sB", _f32()), _ptr(m_indices, "m_indices", (torch.int32,)),
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _scale_types(name)), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", _scale_types(name)), _ptr(m_indices, "m_indices", (torch.int32,)),
                               _ptr(D, "D", _d_types(f32)), M, N, K, G, _stream(stream)))
     return D
 
@@ -182,8 +199,8 @@ def _masked(name, f32, A, sA, B, sB, masked_m, D, stream):
     lib = load()
     G, M_max, K = A.shape
     N = B.shape[1]
-    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
-                              _ptr(sB, "sB", _f32()), _ptr(masked_m, "masked_m", (torch.int32,)),
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _scale_types(name)), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", _scale_types(name)), _ptr(masked_m, "masked_m", (torch.int32,)),
                               _ptr(D, "D", _d_types(f32)), G, M_max, N, K, _stream(stream)))
     return D
 
@@ -195,6 +212,31 @@ def dg_fp8_grouped_masked(A, sA, B, sB, masked_m, D, stream=None):
 
 def dg_fp8_grouped_masked_f32(A, sA, B, sB, masked_m, D, stream=None):
     return _masked("dg_fp8_grouped_masked_f32", True, A, sA, B, sB, masked_m, D, stream)
+
+
+def dg_fp8_gemm_nt_ue8m0(A, sA, B, sB, D, stream=None):
+    """Dense D (bfloat16) with power-of-two scales given as packed UE8M0 int32 words."""
+    return _dense("dg_fp8_gemm_nt_ue8m0", False, A, sA, B, sB, D, stream)
+
+
+def dg_fp8_gemm_nt_ue8m0_f32(A, sA, B, sB, D, stream=None):
+    return _dense("dg_fp8_gemm_nt_ue8m0_f32", True, A, sA, B, sB, D, stream)
+
+
+def dg_fp8_grouped_contiguous_ue8m0(A, sA, B, sB, m_indices, D, stream=None):
+    return _contig("dg_fp8_grouped_contiguous_ue8m0", False, A, sA, B, sB, m_indices, D, stream)
+
+
+def dg_fp8_grouped_contiguous_ue8m0_f32(A, sA, B, sB, m_indices, D, stream=None):
+    return _contig("dg_fp8_grouped_contiguous_ue8m0_f32", True, A, sA, B, sB, m_indices, D, stream)
+
+
+def dg_fp8_grouped_masked_ue8m0(A, sA, B, sB, masked_m, D, stream=None):
+    return _masked("dg_fp8_grouped_masked_ue8m0", False, A, sA, B, sB, masked_m, D, stream)
+
+
+def dg_fp8_grouped_masked_ue8m0_f32(A, sA, B, sB, masked_m, D, stream=None):
+    return _masked("dg_fp8_grouped_masked_ue8m0_f32", True, A, sA, B, sB, masked_m, D, stream)
 
 
 def dg_get_tma_aligned_size(x: int, elem_bytes: int) -> int:
@@ -230,5 +272,13 @@ def dg_query_config(mode: int, M: int, N: int, K: int, G: int = 1, out_f32: bool
     """Tile configuration a call would launch: mode 0 dense, 1 contiguous, 2 masked."""
     cfg = (ctypes.c_int * 6)()
     _check(load().dg_query_config(mode, M, N, K, G, 1 if out_f32 else 0, cfg))
+    keys = ("block_m", "block_n", "stages", "splits", "grid", "tiles")
+    return dict(zip(keys, [int(v) for v in cfg]))
+
+
+def dg_query_config_ue8m0(mode: int, M: int, N: int, K: int, G: int = 1, out_f32: bool = False) -> dict:
+    """Tile configuration of the packed-UE8M0 (block-scaled) calls."""
+    cfg = (ctypes.c_int * 6)()
+    _check(load().dg_query_config_ue8m0(mode, M, N, K, G, 1 if out_f32 else 0, cfg))
     keys = ("block_m", "block_n", "stages", "splits", "grid", "tiles")
     return dict(zip(keys, [int(v) for v in cfg]))

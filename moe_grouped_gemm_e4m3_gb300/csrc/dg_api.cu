@@ -125,14 +125,16 @@ struct Config {
   int raster_m;
 };
 
-Config choose_config(int mode, int rows, int N, int K, int G, int num_sms) {
+Config choose_config(int mode, int rows, int N, int K, int G, int num_sms, bool block_scaled = false) {
   // Cost model calibrated on GB300 (sm_103a), times in microseconds per CTA:
   //  * compute: one K-block (BM=128, BK=128) costs ~0.55 (BN=256) or ~0.50 (BN=128: an N=128 MMA
   //    takes as long as an N=256 one, for half the work);
   //  * memory: a CTA streams ~48 GB/s when its operands come from HBM; operands shared by other
   //    tiles in flight (A across n-blocks, B across m-blocks) come from L2 and cost no HBM time;
   //  * split-K: the last split reads every partial tile back, ~0.6 (BN=128) / ~1.0 (BN=256) per split;
-  //  * a tile's prologue/epilogue: ~1.5.
+  //  * a tile's prologue/epilogue: ~1.5;
+  //  * the block-scaled kernel (packed UE8M0 scales) has no per-K-block promotion: ~0.30 per
+  //    K-block, BN = 256 only.
   // Split-K is considered only while all units fit in one wave (more waves never shorten the
   // critical path). The HBM time of the operands bounds the estimate from below.
   constexpr double kTileUs = 1.5, kCtaGBs = 48.0, kHbmGBs = 6000.0;
@@ -145,11 +147,13 @@ Config choose_config(int mode, int rows, int N, int K, int G, int num_sms) {
   int best_s = 1;
   double best_t = 1e300;
   const int max_s = (mode == dg::kMasked) ? 1 : kMaxSplits;
+  if (block_scaled) bn = 256;
   for (int cand_bn = 128; cand_bn <= 256; cand_bn += 128) {
-    if (cand_bn == 256 && N <= 128) continue;
+    if (cand_bn == 256 && N <= 128 && !block_scaled) continue;
+    if (cand_bn == 128 && block_scaled) continue;
     const int n_blocks = ceil_div(N, cand_bn);
     const int tiles = m_blocks * n_blocks;
-    const double t_compute = cand_bn == 256 ? 0.55 : 0.50;
+    const double t_compute = block_scaled ? 0.30 : (cand_bn == 256 ? 0.55 : 0.50);
     const double t_red = cand_bn == 256 ? 1.0 : 0.6;
     for (int s = 1; s <= max_s; ++s) {
       const int kps = ceil_div(nkb, s);
@@ -175,7 +179,7 @@ Config choose_config(int mode, int rows, int N, int K, int G, int num_sms) {
   // Tuning overrides (environment): DG_BLOCK_N in {128, 256} and DG_SPLITS >= 1 (dense and
   // contiguous only; a split that would exceed one wave of units is still allowed here).
   int bn_final = bn, tiles_final = tiles;
-  if (const char* e = std::getenv("DG_BLOCK_N")) {
+  if (const char* e = block_scaled ? nullptr : std::getenv("DG_BLOCK_N")) {
     const int v = std::atoi(e);
     if (v == 128 || v == 256) { bn_final = v; tiles_final = m_blocks * ceil_div(N, v); }
   }
@@ -188,7 +192,7 @@ Config choose_config(int mode, int rows, int N, int K, int G, int num_sms) {
   c.kb_per_split = ceil_div(nkb, best_s);
   c.splits = ceil_div(nkb, c.kb_per_split);
   c.block_n = bn_final;
-  c.stages = dg::stages_for(bn_final);
+  c.stages = block_scaled ? dg::BsSmemPlan::kStages : dg::stages_for(bn_final);
   c.tiles = tiles_final;
   const long long units = (long long)tiles_final * c.splits;
   c.grid = (int)(units < num_sms ? units : num_sms);
@@ -251,8 +255,11 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Common implementation of the six GEMM entry points.
 //   mode dense: rows = M, G = 1;  contiguous: rows = M_total;  masked: rows = M_max (per group).
-dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
-                   const int32_t* idx, void* D, int rows, int N, int K, int G, cudaStream_t stream) {
+//   sA/sB are FP32 scales, or (block_scaled) packed UE8M0 words: sA [G][ceil(nkb/4)][ldsa] and
+//   sB [G][nnb][ceil(nkb/4)] int32.
+dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, const uint8_t* B, const void* sB,
+                   const int32_t* idx, void* D, int rows, int N, int K, int G, cudaStream_t stream,
+                   bool block_scaled = false) {
   t_last_error.clear();
   if (rows < 0 || N < 0 || K < 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
   if (mode != dg::kDense && G < 1 && rows > 0) {
@@ -279,7 +286,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const float* sA, co
   dg_status s = device_state(&st);
   if (s != DG_OK) return s;
   const int sms = effective_sms(*st);
-  const Config cfg = choose_config(mode, rows, N, K, mode == dg::kDense ? 1 : G, sms);
+  const Config cfg = choose_config(mode, rows, N, K, mode == dg::kDense ? 1 : G, sms, block_scaled);
   if ((long long)cfg.tiles * cfg.splits > INT_MAX / 2) return fail(DG_ERR_UNSUPPORTED, "too many tiles");
 
   dg::LaunchArgs a;
@@ -298,8 +305,14 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const float* sA, co
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles * cfg.splits;
   p.raster_m = cfg.raster_m;
-  p.sA = sA;
-  p.sB = sB;
+  p.nkq = ceil_div(p.nkb, 4);
+  if (block_scaled) {
+    p.sfa = static_cast<const uint32_t*>(sA);
+    p.sfb = static_cast<const uint32_t*>(sB);
+  } else {
+    p.sA = static_cast<const float*>(sA);
+    p.sB = static_cast<const float*>(sB);
+  }
   p.m_indices = mode == dg::kContiguous ? idx : nullptr;
   p.masked_m = mode == dg::kMasked ? idx : nullptr;
   p.D = D;
@@ -332,11 +345,16 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const float* sA, co
   a.stream = stream;
   if (print_configs()) {
     static const char* names[3] = {"dense", "contiguous", "masked"};
-    std::fprintf(stderr, "[dg] %s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d grid=%d tiles=%d\n",
-                 names[mode], out_f32 ? "/f32" : "", rows, N, K, p.G, cfg.block_n, cfg.stages, cfg.splits, cfg.grid,
-                 cfg.tiles);
+    std::fprintf(stderr, "[dg] %s%s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d grid=%d tiles=%d\n",
+                 names[mode], block_scaled ? "/ue8m0" : "", out_f32 ? "/f32" : "", rows, N, K, p.G, cfg.block_n,
+                 cfg.stages, cfg.splits, cfg.grid, cfg.tiles);
   }
   cudaError_t e;
+  if (block_scaled) {
+    e = dg::launch_bs(a, static_cast<dg::Mode>(mode));
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return DG_OK;
+  }
   switch (mode) {
     case dg::kDense: e = dg::launch_dense(a); break;
     case dg::kContiguous: e = dg::launch_contiguous(a); break;
@@ -384,6 +402,44 @@ dg_status dg_fp8_grouped_masked_f32(const uint8_t* A, const float* sA, const uin
                                     const int32_t* masked_m, float* D, int G, int M_max, int N, int K,
                                     dg_stream_t stream) {
   return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_gemm_nt_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB, uint16_t* D,
+                               int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true);
+}
+
+dg_status dg_fp8_gemm_nt_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB, float* D,
+                                   int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true);
+}
+
+dg_status dg_fp8_grouped_contiguous_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                          const int32_t* m_indices, uint16_t* D, int M_total, int N, int K, int G,
+                                          dg_stream_t stream) {
+  return run_gemm(dg::kContiguous, false, A, sA, B, sB, m_indices, D, M_total, N, K, G,
+                  static_cast<cudaStream_t>(stream), true);
+}
+
+dg_status dg_fp8_grouped_contiguous_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                              const int32_t* sB, const int32_t* m_indices, float* D, int M_total,
+                                              int N, int K, int G, dg_stream_t stream) {
+  return run_gemm(dg::kContiguous, true, A, sA, B, sB, m_indices, D, M_total, N, K, G,
+                  static_cast<cudaStream_t>(stream), true);
+}
+
+dg_status dg_fp8_grouped_masked_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                      const int32_t* masked_m, uint16_t* D, int G, int M_max, int N, int K,
+                                      dg_stream_t stream) {
+  return run_gemm(dg::kMasked, false, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream),
+                  true);
+}
+
+dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                          const int32_t* masked_m, float* D, int G, int M_max, int N, int K,
+                                          dg_stream_t stream) {
+  return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream),
+                  true);
 }
 
 int dg_get_tma_aligned_size(int x, int elem_bytes) {
@@ -438,15 +494,16 @@ dg_status dg_get_device_status(int* code, dg_stream_t stream) {
 
 const char* dg_last_error_string(void) { return t_last_error.c_str(); }
 
-dg_status dg_query_config(int mode, int M, int N, int K, int G, int out_f32, int* cfg) {
+namespace {
+
+dg_status query_config(int mode, int M, int N, int K, int G, int* cfg, bool block_scaled) {
   t_last_error.clear();
-  (void)out_f32;  // the configuration never depends on the output type
   if (!cfg || mode < 0 || mode > 2 || M < 0 || N < 0 || K <= 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "bad query");
   DeviceState* st = nullptr;
   int sms = num_sms_cap();
   if (device_state(&st) == DG_OK) sms = effective_sms(*st);
   if (sms <= 0) sms = 152;  // no device: report the GB300 configuration
-  const Config c = choose_config(mode, M, N, K, mode == 0 ? 1 : G, sms);
+  const Config c = choose_config(mode, M, N, K, mode == 0 ? 1 : G, sms, block_scaled);
   cfg[0] = 128;
   cfg[1] = c.block_n;
   cfg[2] = c.stages;
@@ -454,6 +511,18 @@ dg_status dg_query_config(int mode, int M, int N, int K, int G, int out_f32, int
   cfg[4] = c.grid;
   cfg[5] = c.tiles;
   return DG_OK;
+}
+
+}  // namespace
+
+dg_status dg_query_config(int mode, int M, int N, int K, int G, int out_f32, int* cfg) {
+  (void)out_f32;  // the configuration never depends on the output type
+  return query_config(mode, M, N, K, G, cfg, false);
+}
+
+dg_status dg_query_config_ue8m0(int mode, int M, int N, int K, int G, int out_f32, int* cfg) {
+  (void)out_f32;
+  return query_config(mode, M, N, K, G, cfg, true);
 }
 
 }  // extern "C"

@@ -63,6 +63,9 @@ struct GemmParams {
   int raster_m;      // m-blocks per rasterisation group
   const float* sA;
   const float* sB;
+  const uint32_t* sfa;  // packed UE8M0 scales (block-scaled kernel): [G][ceil(nkb/4)][ldsa]
+  const uint32_t* sfb;  // packed UE8M0 scales (block-scaled kernel): [G][nnb][ceil(nkb/4)]
+  int nkq;              // ceil(nkb / 4): packed scale words along K
   const int32_t* m_indices;
   const int32_t* masked_m;
   void* D;           // row-major, row stride N elements (used by predicated stores)

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "dg_kernel.cuh"
+#include "dg_kernel_bs.cuh"
 
 namespace dg {
 
@@ -31,6 +32,8 @@ constexpr int tmem_bufs_for(int block_n) { return 512 / block_n; }
 cudaError_t launch_dense(const LaunchArgs& a);
 cudaError_t launch_contiguous(const LaunchArgs& a);
 cudaError_t launch_masked(const LaunchArgs& a);
+// The block-scaled kernel for packed UE8M0 scales (block_n is always 256).
+cudaError_t launch_bs(const LaunchArgs& a, Mode mode);
 
 // Launches one instantiation; sets its dynamic shared-memory limit on first use per device.
 template <int BN, Mode MODE, bool OUT_F32>
@@ -52,6 +55,23 @@ cudaError_t launch_instance(const LaunchArgs& a) {
     configured[dev] = true;
   }
   kernel<<<a.grid, R::kThreads, Plan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
+  return cudaGetLastError();
+}
+
+template <Mode MODE, bool OUT_F32>
+cudaError_t launch_bs_instance(const LaunchArgs& a) {
+  auto kernel = fp8_gemm_bs_kernel<MODE, OUT_F32>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BsSmemPlan::kDynamicBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  kernel<<<a.grid, BsRoles::kThreads, BsSmemPlan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
   return cudaGetLastError();
 }
 

@@ -220,6 +220,49 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: E4M3 A and B (formats [7,10) and
+// [10,13) = 0), both K-major, FP32 accumulator, N >> 3 at [17,23), scale-factor type UE8M0 at bit
+// 23, M >> 7 at [27,29). The scale-factor IDs (which byte of the 32-bit TMEM cell the MMA reads:
+// B at [4,6), A at [29,31)) are added per K-block.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3_bs(uint32_t M, uint32_t N) {
+  return ((N >> 3) << 17) | (1u << 23) | ((M >> 7) << 27);
+}
+
+__host__ __device__ constexpr uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t sf_id) {
+  return idesc | (sf_id << 29) | (sf_id << 4);
+}
+
+// D(tmem) (+)= (A·sfA)(smem) · (B·sfB)(smem)ᵀ for one K=32 step of E4M3 operands, each row of A and
+// of B multiplied by its UE8M0 scale factor read from TMEM (one scale per 32 K-elements:
+// scale_vec::1X). Issued by one thread.
+__device__ __forceinline__ void mma_e4m3_block_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                      uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Stores one 32-bit column of this warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+// Stores eight consecutive 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3,
+                                                  uint32_t v4, uint32_t v5, uint32_t v6, uint32_t v7) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(v0),
+               "r"(v1), "r"(v2), "r"(v3), "r"(v4), "r"(v5), "r"(v6), "r"(v7)
+               : "memory");
+}
+
+// Waits until this thread's tcgen05.st have completed.
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Loads 32 consecutive FP32 columns of this warp's 32 TMEM lanes (one lane per thread).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
