@@ -11,7 +11,11 @@ Metric: useful TFLOP/s = sum(2*M*N*K) / sum(GEMM time). Printed as one JSON line
 roofline of the dominant kernel, the CPU oracle baseline, the end-to-end number through host
 buffers, the SM clocks seen during the timed region and the number of kernel launches.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--scales fp32|ue8m0]
+
+``--scales ue8m0`` runs the same workload with power-of-two scales (the smallest 2^p >= amax/448)
+packed as UE8M0 words through the block-scaled entry points; the default, fp32, is the amax/448
+FP32-scale GEMM with CUDA-core promotion.
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs the same sweep on its own GPU (replicas,
 weak scaling); rank 0 prints the whole-job throughput using the slowest rank's time.
@@ -43,6 +47,7 @@ WORKLOAD = "dense FP8 E4M3 GEMM sweep, M in {64,128,4096} x (N,K) in {(2112,7168
 METRIC = "FP8 TFLOPS (2MNK/s) per shape; % of GB300 FP8 dense peak or HBM GB/s"
 L2_FLUSH_BYTES = 256 << 20
 CPU_SAMPLE_PER_SHAPE = 196608
+UE8M0 = False      # set by --scales ue8m0
 
 
 def parse_args():
@@ -59,7 +64,12 @@ def parse_args():
                          "and print one JSON line per shape instead of the benchmark line")
     ap.add_argument("--shapes", default=None,
                     help="restrict the sweep to these MxNxK shapes (comma-separated), e.g. for profiling")
+    ap.add_argument("--scales", choices=["fp32", "ue8m0"], default="fp32",
+                    help="fp32: amax/448 FP32 scales (CUDA-core promotion); ue8m0: power-of-two scales packed "
+                         "as UE8M0 (block-scaled tensor-core kernel)")
     args = ap.parse_args()
+    global UE8M0
+    UE8M0 = args.scales == "ue8m0"
     if args.shapes:
         global SHAPES
         SHAPES = [tuple(int(v) for v in s.lower().split("x")) for s in args.shapes.split(",")]
@@ -78,8 +88,34 @@ def load_peaks():
 
 
 def algorithmic_bytes(M, N, K):
+    """Bytes one dense GEMM must move: A, B, their scales (FP32, or UE8M0 packed four K-groups
+    to an int32) and the BF16 D."""
     nkb, nnb = -(-K // 128), -(-N // 128)
-    return M * K + N * K + 4 * M * nkb + 4 * nnb * nkb + 2 * M * N
+    nks = -(-nkb // 4) if UE8M0 else nkb
+    return M * K + N * K + 4 * M * nks + 4 * nnb * nks + 2 * M * N
+
+
+def gpu_scales(a, b):
+    """The scale arrays a GEMM call takes: FP32, or packed UE8M0 words."""
+    import dg_inputs
+    if UE8M0:
+        return dg_inputs.pack_ue8m0_a(a.sA), dg_inputs.pack_ue8m0_b(b.sB)
+    return a.sA, b.sB
+
+
+def gemm_entry(dg, kind="dense"):
+    names = {"dense": "dg_fp8_gemm_nt", "contiguous": "dg_fp8_grouped_contiguous", "masked": "dg_fp8_grouped_masked"}
+    return getattr(dg, names[kind] + ("_ue8m0" if UE8M0 else ""))
+
+
+def query_config(dg, *a):
+    return (dg.dg_query_config_ue8m0 if UE8M0 else dg.dg_query_config)(*a)
+
+
+def quantisation_note():
+    if UE8M0:
+        return "E4M3, A 1x128 / B 128x128 power-of-two scales (smallest 2^p >= amax/448), packed UE8M0"
+    return "E4M3, A 1x128 / B 128x128 FP32 scales, amax/448"
 
 
 def measured_traffic(shape: str):
@@ -97,7 +133,7 @@ def measured_traffic(shape: str):
             h.update(f.read())
     if h.hexdigest() != rec.get("source_sha256"):
         return None
-    launch = rec.get("launches", {}).get(shape)
+    launch = rec.get("launches_ue8m0" if UE8M0 else "launches", {}).get(shape)
     if not launch:
         return None
     return int(launch["dram_read_bytes"] + launch["dram_write_bytes"])
@@ -119,9 +155,9 @@ def make_inputs():
     a_cache, b_cache, out = {}, {}, []
     for (M, N, K) in SHAPES:
         if (M, K) not in a_cache:
-            a_cache[(M, K)] = dg_inputs.make_a(M, K, seed=0)
+            a_cache[(M, K)] = dg_inputs.make_a(M, K, seed=0, ue8m0=UE8M0)
         if (N, K) not in b_cache:
-            b_cache[(N, K)] = dg_inputs.make_b(1, N, K, seed=0)
+            b_cache[(N, K)] = dg_inputs.make_b(1, N, K, seed=0, ue8m0=UE8M0)
         out.append((M, N, K, a_cache[(M, K)], b_cache[(N, K)]))
     return out
 
@@ -227,10 +263,12 @@ def run_ours(args, rank, world, local):
     problems = make_inputs()
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     tensors = []
+    gemm = gemm_entry(dg)
     for (M, N, K, a, b) in problems:
-        tensors.append(dict(M=M, N=N, K=K, A=dev(a.A), sA=dev(a.sA), B=dev(b.B[0]), sB=dev(b.sB[0]),
+        gsA, gsB = gpu_scales(a, b)
+        tensors.append(dict(M=M, N=N, K=K, A=dev(a.A), sA=dev(gsA), B=dev(b.B[0]), sB=dev(gsB[0]),
                             D=torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
-                            cfg=dg.dg_query_config(0, M, N, K)))
+                            cfg=query_config(dg, 0, M, N, K)))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -239,7 +277,7 @@ def run_ours(args, rank, world, local):
             flush.fill_(i & 0xFF)
             if events is not None:
                 events[i][0].record(stream)
-            dg.dg_fp8_gemm_nt(t["A"], t["sA"], t["B"], t["sB"], t["D"], stream)
+            gemm(t["A"], t["sA"], t["B"], t["sB"], t["D"], stream)
             if events is not None:
                 events[i][1].record(stream)
 
@@ -330,7 +368,8 @@ def run_ours(args, rank, world, local):
     l_ms = float(mean_ms[li])
     l_flops = 2.0 * lt["M"] * lt["N"] * lt["K"]
     l_bytes = algorithmic_bytes(lt["M"], lt["N"], lt["K"])
-    kname = f"fp8_gemm_kernel<BN={dom_key[0]},{'split-K' if dom_key[1] else 'no split'},dense,bf16>"
+    kname = (f"fp8_gemm_bs_kernel<dense,bf16> ({'split-K' if dom_key[1] else 'no split'}, BN=256)" if UE8M0 else
+             f"fp8_gemm_kernel<BN={dom_key[0]},{'split-K' if dom_key[1] else 'no split'},dense,bf16>")
     if l_flops / (fp8_peak * 1e12) >= l_bytes / (peaks["hbm_gbs"] * 1e9):
         achieved = l_flops / (l_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
@@ -353,9 +392,11 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate (fine-grained scales) -> bf16", "data": "synthetic",
+        "vs_baseline": None, "data": "synthetic",
+        "dtype": ("e4m3 x e4m3 block-scaled by ue8m0 -> f32 accumulate -> bf16" if UE8M0 else
+                  "e4m3 x e4m3 -> f32 accumulate (fine-grained scales) -> bf16"),
         "config": {"workload": WORKLOAD if len(tensors) == 18 else f"subset {SHAPES}", "shapes": len(tensors), "seed": 0, "values": "N(0,1)",
-                   "quantisation": "E4M3, A 1x128 / B 128x128 FP32 scales, amax/448",
+                   "quantisation": quantisation_note(),
                    "l2": "256 MB write before every GEMM, outside the GEMM's CUDA events",
                    "parallelism": f"replicas x{world}", "wall_ms_per_step": round((t1 - t0) * 1e3 / args.steps, 4)},
         "roofline": roof,
@@ -376,9 +417,11 @@ def measure_e2e(dg, problems, args, stream):
     import torch
     host = []
     h2d = d2h = 0
+    gemm = gemm_entry(dg)
     for (M, N, K, a, b) in problems:
         h = dict(M=M, N=N, K=K)
-        for name, arr in (("A", a.A), ("sA", a.sA), ("B", b.B[0]), ("sB", b.sB[0])):
+        gsA, gsB = gpu_scales(a, b)
+        for name, arr in (("A", a.A), ("sA", gsA), ("B", b.B[0]), ("sB", gsB[0])):
             ht = torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
             h[name] = ht
             h["d" + name] = torch.empty_like(ht, device="cuda")
@@ -397,7 +440,7 @@ def measure_e2e(dg, problems, args, stream):
                 evs[i][0].record(stream)
             for name in ("A", "sA", "B", "sB"):
                 h["d" + name].copy_(h[name], non_blocking=True)
-            dg.dg_fp8_gemm_nt(h["dA"], h["dsA"], h["dB"], h["dsB"], h["dD"], stream)
+            gemm(h["dA"], h["dsA"], h["dB"], h["dsB"], h["dD"], stream)
             h["D"].copy_(h["dD"], non_blocking=True)
             if evs is not None:
                 evs[i][1].record(stream)
@@ -420,13 +463,26 @@ def measure_e2e(dg, problems, args, stream):
 # CPU oracle (baseline and the reference arm)
 
 
+def oracle_scales(a, b, K):
+    """The FP32 scales the oracle uses: the arrays themselves, or the UE8M0 words the GPU gets,
+    unpacked by the oracle."""
+    if not UE8M0:
+        return a.sA, b.sB
+    import oracle
+    pa, pb = gpu_scales(a, b)
+    nkb = -(-K // 128)
+    return oracle.unpack_ue8m0_a(pa, nkb), oracle.unpack_ue8m0_b(pb, nkb)
+
+
 def cpu_sample_plan(problems, per_shape, seed=0):
+    import dg_inputs
     rng = np.random.default_rng(seed)
     plan = []
     for (M, N, K, a, b) in problems:
         ms = rng.integers(0, M, per_shape)
         ns = rng.integers(0, N, per_shape)
-        plan.append((M, N, K, a, b, ms, ns))
+        sA, sB = oracle_scales(a, b, K)
+        plan.append((M, N, K, dg_inputs.OperandA(a.A, sA), dg_inputs.OperandB(b.B, sB), ms, ns))
     return plan
 
 
@@ -530,13 +586,18 @@ def run_all_configs(args):
         line.update(extra or {})
         print(json.dumps(line), flush=True)
 
+    scales = {"scales": "ue8m0" if UE8M0 else "fp32"}
+
     def dense(config, M, N, K, dist=dg_inputs.NORMAL, outliers=0.0):
-        a = dg_inputs.make_a(M, K, seed=0, dist=dist, outlier_frac=outliers)
-        b = dg_inputs.make_b(1, N, K, seed=0, dist=dist)
-        A, sA, B, sB = dev(a.A), dev(a.sA), dev(b.B[0]), dev(b.sB[0])
+        a = dg_inputs.make_a(M, K, seed=0, dist=dist, outlier_frac=outliers, ue8m0=UE8M0)
+        b = dg_inputs.make_b(1, N, K, seed=0, dist=dist, ue8m0=UE8M0)
+        gsA, gsB = gpu_scales(a, b)
+        A, sA, B, sB = dev(a.A), dev(gsA), dev(b.B[0]), dev(gsB[0])
         D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-        ms = timeit(lambda: dg.dg_fp8_gemm_nt(A, sA, B, sB, D))
-        report(config, f"{M}x{N}x{K}", 2.0 * M * N * K, algorithmic_bytes(M, N, K), ms, {"cfg": dg.dg_query_config(0, M, N, K)})
+        gemm = gemm_entry(dg)
+        ms = timeit(lambda: gemm(A, sA, B, sB, D))
+        report(config, f"{M}x{N}x{K}", 2.0 * M * N * K, algorithmic_bytes(M, N, K), ms,
+               dict(scales, cfg=query_config(dg, 0, M, N, K)))
 
     dense("1 dense small", 128, 512, 1024)
     for (M, N, K) in [(M, N, K) for M in SWEEP_M for (N, K) in SWEEP_NK]:
@@ -544,29 +605,37 @@ def run_all_configs(args):
     for G in (4, 8):
         for (N, K) in ((4096, 7168), (7168, 2048)):
             M = G * 8192
-            a = dg_inputs.make_a(M, K, seed=0)
-            b = dg_inputs.make_b(G, N, K, seed=0)
+            a = dg_inputs.make_a(M, K, seed=0, ue8m0=UE8M0)
+            b = dg_inputs.make_b(G, N, K, seed=0, ue8m0=UE8M0)
+            gsA, gsB = gpu_scales(a, b)
             idx = dev(np.repeat(np.arange(G, dtype=np.int32), 8192))
-            A, sA, B, sB = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB)
+            A, sA, B, sB = dev(a.A), dev(gsA), dev(b.B), dev(gsB)
             D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-            ms = timeit(lambda: dg.dg_fp8_grouped_contiguous(A, sA, B, sB, idx, D))
+            gemm = gemm_entry(dg, "contiguous")
+            ms = timeit(lambda: gemm(A, sA, B, sB, idx, D))
             nkb, nnb = -(-K // 128), -(-N // 128)
-            nbytes = M * K + G * N * K + 4 * M * nkb + 4 * G * nnb * nkb + 2 * M * N
-            report("3 contiguous", f"G={G} M={M} N={N} K={K}", 2.0 * M * N * K, nbytes, ms)
+            nks = -(-nkb // 4) if UE8M0 else nkb
+            nbytes = M * K + G * N * K + 4 * M * nks + 4 * G * nnb * nks + 2 * M * N
+            report("3 contiguous", f"G={G} M={M} N={N} K={K}", 2.0 * M * N * K, nbytes, ms,
+                   dict(scales, cfg=query_config(dg, 1, M, N, K, G)))
             del A, B, D
     for (N, K) in ((4096, 7168), (7168, 2048)):
         G, M_max = 16, 256
         mm = dg_inputs.make_masked_m(G, M_max, seed=0)
-        a = dg_inputs.make_masked_a(G, M_max, K, seed=0)
-        b = dg_inputs.make_b(G, N, K, seed=0)
-        A, sA, B, sB, MM = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(mm)
+        a = dg_inputs.make_masked_a(G, M_max, K, seed=0, ue8m0=UE8M0)
+        b = dg_inputs.make_b(G, N, K, seed=0, ue8m0=UE8M0)
+        gsA, gsB = gpu_scales(a, b)
+        A, sA, B, sB, MM = dev(a.A), dev(gsA), dev(b.B), dev(gsB), dev(mm)
         D = torch.empty(G, M_max, N, dtype=torch.bfloat16, device="cuda")
-        ms = timeit(lambda: dg.dg_fp8_grouped_masked(A, sA, B, sB, MM, D))
+        gemm = gemm_entry(dg, "masked")
+        ms = timeit(lambda: gemm(A, sA, B, sB, MM, D))
         valid = int(mm.sum())
         nkb, nnb = -(-K // 128), -(-N // 128)
+        nks = -(-nkb // 4) if UE8M0 else nkb
         active = int((mm > 0).sum())
-        nbytes = valid * K + active * N * K + 4 * valid * nkb + 4 * G * nnb * nkb + 2 * valid * N
-        report("4 masked", f"G=16 M_max=256 sum(masked_m)={valid} N={N} K={K}", 2.0 * valid * N * K, nbytes, ms)
+        nbytes = valid * K + active * N * K + 4 * valid * nks + 4 * G * nnb * nks + 2 * valid * N
+        report("4 masked", f"G=16 M_max=256 sum(masked_m)={valid} N={N} K={K}", 2.0 * valid * N * K, nbytes, ms,
+               dict(scales, cfg=query_config(dg, 2, M_max, N, K, G)))
     for (M, N, K) in ((4096, 2112, 7168), (4096, 576, 7168), (4096, 7168, 32768)):
         dense("5 stress (Student-t, outliers)", M, N, K, dist=dg_inputs.STUDENT_T3, outliers=0.01)
 
