@@ -53,6 +53,7 @@ def _load():
         lib.dgo_grouped_masked.restype = i32
         lib.dgo_grouped_masked.argtypes = [P, P, i64, P, P, P, i32, i32, i32, i32, P, P, i32]
         lib.dgo_gemm_nt_sampled.argtypes = [P, P, i64, P, P, i32, i32, i32, i64, P, P, P, i32]
+        lib.dgo_gemm_nt_acc.argtypes = [P, P, i64, P, P, P, i32, i32, i32, P, i32]
         lib.dgo_hardware_threads.restype = i32
         lib.dgo_ue8m0_decode.restype = ctypes.c_double
         lib.dgo_ue8m0_decode.argtypes = [ctypes.c_uint8]
@@ -113,6 +114,27 @@ def gemm_nt(A, sA, B, sB, threads=None, want_ref64=True, want_bf16=True):
                         _p(ref) if ref is not None else None, _p(D) if D is not None else None,
                         _threads(threads))
     return ref, D
+
+
+def gemm_nt_acc(A, sA, B, sB, C, threads=None) -> np.ndarray:
+    """Accumulating dense D = C + A·Bᵀ in FP64 (C float32 [M,N]). Returns ref64 [M,N]."""
+    A, B, sA, sB = _u8(A), _u8(B), _f32(sA), _f32(sB)
+    if B.ndim == 3:
+        B, sB = B[0], sB[0]
+    C = _f32(C)
+    M, K = A.shape
+    N = B.shape[0]
+    assert C.shape == (M, N)
+    ref = np.empty((M, N), np.float64)
+    _load().dgo_gemm_nt_acc(_p(A), _p(sA), sA.shape[-1], _p(B), _p(sB), _p(C), M, N, K, _p(ref), _threads(threads))
+    return ref
+
+
+def gemm_nt_acc_sampled(A, sA, B, sB, C, ms, ns, threads=None) -> np.ndarray:
+    """FP64 values of sampled elements of D = C + A·Bᵀ."""
+    ms = np.asarray(ms, np.int64)
+    ns = np.asarray(ns, np.int64)
+    return np.asarray(C, np.float32)[ms, ns].astype(np.float64) + gemm_nt_sampled(A, sA, B, sB, ms, ns, threads)
 
 
 def grouped_contiguous(A, sA, B, sB, m_indices, ref64_init=None, D_init=None, threads=None):

@@ -31,6 +31,8 @@
 //     bits; exponent field 15 with mantissa 7 is NaN; no infinities; largest finite value 448).
 //   * BF16 output rounding: IEEE round-to-nearest-even, taken directly from the FP64 value (no
 //     intermediate FP32 rounding).
+//   * Accumulating form D = C + A @ B.T (the kernel naming D = C + A @ B and fp8_gemm_nt's
+//     definition, same page and section): C is an FP32 [M,N] matrix added to the FP64 GEMM value.
 //   * Packed UE8M0 scales (the Blackwell input form): the SM100 implementation takes its scaling
 //     factors as UE8M0 values, four of them packed into one 32-bit integer (same page, § "GEMM
 //     arayüzü ve yerleşim kısıtları"). UE8M0 is the OCP Microscaling (MX) v1.0 E8M0 format
@@ -162,6 +164,20 @@ void dgo_bf16_from_f64_array(const double* x, uint16_t* out, int64_t n) {
 void dgo_gemm_nt(const uint8_t* A, const float* sA, int64_t ldsa, const uint8_t* B, const float* sB,
                  int M, int N, int K, double* ref64, uint16_t* D, int threads) {
   dense_rows(A, sA, ldsa, B, sB, M, N, K, ref64, D, threads);
+}
+
+// Dense accumulating D = C + A[M,K]·B[N,K]ᵀ: ref64[m,n] = C[m,n] + (the dense value above), in
+// FP64 (C, FP32, is exact in FP64).
+void dgo_gemm_nt_acc(const uint8_t* A, const float* sA, int64_t ldsa, const uint8_t* B, const float* sB,
+                     const float* C, int M, int N, int K, double* ref64, int threads) {
+  const int nkb = ceil_div(K, 128);
+  parallel_rows(M, threads, [&](int m) {
+    for (int n = 0; n < N; ++n) {
+      const double v = element(A + (int64_t)m * K, sA + m, ldsa, B + (int64_t)n * K,
+                               sB + (int64_t)(n / 128) * nkb, K);
+      ref64[(int64_t)m * N + n] = (double)C[(int64_t)m * N + n] + v;
+    }
+  });
 }
 
 // Contiguous grouped: A[M_total,K], sA[nkb][ldsa], B[G,N,K], sB[G][nnb][nkb], m_indices[M_total].

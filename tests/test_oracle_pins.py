@@ -9,6 +9,8 @@
   random inputs (pins the scale indexing); identity B; scale linearity; a single K-block.
 * Grouped forms: contiguous and masked equal the dense oracle per group, bit for bit, and rows
   outside the valid region stay untouched.
+* Accumulating form D = C + A·Bᵀ: the hand-worked example with a C added, A = 0 gives C exactly,
+  C = 0 gives the plain GEMM bit for bit.
 * Packed UE8M0 scales: the OCP MX E8M0 table (golden file) and torch's float8_e8m0fnu conversion
   for all 256 codes; a GEMM with packed scales worked by hand (golden file, pins the byte order
   and both packed layouts); the unpacker against the input generator's independent packer; the
@@ -423,3 +425,32 @@ def test_ue8m0_gemm_matches_dequantised_definition(M, N, K, dist):
     want = _numpy_definition(a.A, a.sA, b.B[0], b.sB[0])
     scale = np.abs(want).max()
     assert np.abs(ref64 - want).max() <= 1e-13 * scale
+
+
+# ----------------------------------------------------------------------------------------------
+# Accumulating form D = C + A·Bᵀ
+
+
+def test_gemm_acc_worked_example_by_hand():
+    # The 2x2 example above (A·Bᵀ = [[192, 0], [4224, 0]]) plus C = [[1, 2], [3, 4]].
+    A = np.array([[0x38] * 256, [0x40] * 256], np.uint8)
+    B = np.array([[0x30] * 256, [0x38, 0xB8] * 128], np.uint8)
+    sA = np.array([[1.0, 0.5, 0, 0], [0.25, 8.0, 0, 0]], np.float32)
+    sB = np.array([[2.0, 4.0]], np.float32)
+    C = np.array([[1.0, 2.0], [3.0, 4.0]], np.float32)
+    assert oracle.gemm_nt_acc(A, sA, B, sB, C, threads=1).tolist() == [[193.0, 2.0], [4227.0, 4.0]]
+
+
+def test_gemm_acc_reduces_to_its_parts():
+    M, N, K = 37, 200, 640
+    a = dg_inputs.make_a(M, K, seed=14)
+    b = dg_inputs.make_b(1, N, K, seed=14)
+    C = dg_inputs.draw(14, 5, M * N).reshape(M, N) * 100
+    ref, _ = oracle.gemm_nt(a.A, a.sA, b.B[0], b.sB[0], threads=2)
+    assert np.array_equal(oracle.gemm_nt_acc(a.A, a.sA, b.B[0], b.sB[0], np.zeros_like(C), threads=2), ref)
+    zero_a = np.zeros_like(a.A)
+    assert np.array_equal(oracle.gemm_nt_acc(zero_a, a.sA, b.B[0], b.sB[0], C, threads=2), C.astype(np.float64))
+    rng = np.random.default_rng(1)
+    ms, ns = rng.integers(0, M, 100), rng.integers(0, N, 100)
+    full = oracle.gemm_nt_acc(a.A, a.sA, b.B[0], b.sB[0], C, threads=2)
+    assert np.array_equal(oracle.gemm_nt_acc_sampled(a.A, a.sA, b.B[0], b.sB[0], C, ms, ns), full[ms, ns])
