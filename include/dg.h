@@ -162,6 +162,22 @@ dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, c
                                           int N, int K, dg_stream_t stream);
 
 /*
+ * Accumulating dense GEMM: D = C + A·Bᵀ, the full definition of fp8_gemm_nt ("DeepGEMM: İnce
+ * ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri", tr.news.hada.io/topic?id=19459,
+ * § "GEMM arayüzü ve yerleşim kısıtları": the kernels are named after D = C + A @ B, and
+ * fp8_gemm_nt computes D = C + A @ B.T). C and D are FP32 [M,N] row-major. C may be D itself (in-place
+ * accumulation, e.g. of weight gradients); otherwise C is copied into D on `stream` first, and C and D
+ * must not overlap. Each element of D receives the product exactly once (a TMA reduce-add onto D),
+ * so D = fl32(C + fl32(A·Bᵀ)) and the result is deterministic. The other arguments, layouts and
+ * errors are those of dg_fp8_gemm_nt_f32 (or dg_fp8_gemm_nt_ue8m0_f32 for packed UE8M0 scales).
+ */
+dg_status dg_fp8_gemm_nt_acc_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                 const float* C, float* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_nt_ue8m0_acc_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                       const int32_t* sB, const float* C, float* D, int M, int N, int K,
+                                       dg_stream_t stream);
+
+/*
  * Allocation-free dense GEMM: the same computation, arguments and result as dg_fp8_gemm_nt (the
  * same kernel, tile configuration and accumulation order), for callers that cannot let a library
  * call cudaMalloc — for example a framework whose caching allocator already owns the device memory,

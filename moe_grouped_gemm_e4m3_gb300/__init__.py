@@ -10,6 +10,7 @@ The names mirror the C ABI:
 * ``dg_fp8_grouped_contiguous(A, sA, B, sB, m_indices, D)``  M-grouped, contiguous layout
 * ``dg_fp8_grouped_masked(A, sA, B, sB, masked_m, D)``       M-grouped, masked layout
 * ``*_f32`` variants store the FP32 accumulator instead of BF16 (same kernel and order).
+* ``dg_fp8_gemm_nt_acc_f32(A, sA, B, sB, C, D)``             D = C + A·Bᵀ (FP32 C and D; C may be D)
 * ``*_ue8m0`` variants take power-of-two scales as packed UE8M0 int32 words (four K-groups per
   word, byte j = K-group 4q+j): sA int32 [ceil(ceil(K/128)/4), align4(rows)] (masked: leading G),
   sB int32 [G, ceil(N/128), ceil(ceil(K/128)/4)]. They run the block-scaled tensor-core kernel.
@@ -33,7 +34,7 @@ __all__ = [
     "dg_get_num_sms", "dg_get_device_status", "dg_last_error_string", "dg_query_config",
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
-    "dg_query_config_ue8m0", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
+    "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
     "DG_DEV_TIMEOUT",
 ]
@@ -49,7 +50,7 @@ EXPORTED_SYMBOLS = (
     "dg_last_error_string", "dg_query_config", "dg_fp8_gemm_nt_noalloc",
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
-    "dg_query_config_ue8m0",
+    "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
 )
 
 
@@ -93,6 +94,9 @@ def load(build_if_missing: bool = True):
     lib.dg_get_num_sms.restype, lib.dg_get_num_sms.argtypes = i32, []
     lib.dg_get_device_status.restype, lib.dg_get_device_status.argtypes = i32, [ctypes.POINTER(i32), P]
     lib.dg_last_error_string.restype, lib.dg_last_error_string.argtypes = ctypes.c_char_p, []
+    for name in ("dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, P]
     for name in ("dg_query_config", "dg_query_config_ue8m0"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
@@ -212,6 +216,26 @@ def dg_fp8_grouped_masked(A, sA, B, sB, masked_m, D, stream=None):
 
 def dg_fp8_grouped_masked_f32(A, sA, B, sB, masked_m, D, stream=None):
     return _masked("dg_fp8_grouped_masked_f32", True, A, sA, B, sB, masked_m, D, stream)
+
+
+def _dense_acc(name, A, sA, B, sB, C, D, stream):
+    lib = load()
+    M, K = A.shape
+    N = B.shape[-2]
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _scale_types(name)),
+                              _ptr(B, "B", _fp8_types()), _ptr(sB, "sB", _scale_types(name)), _ptr(C, "C", _f32()),
+                              _ptr(D, "D", _f32()), M, N, K, _stream(stream)))
+    return D
+
+
+def dg_fp8_gemm_nt_acc_f32(A, sA, B, sB, C, D, stream=None):
+    """D (float32) = C + A·Bᵀ; C (float32 [M,N]) may be D itself."""
+    return _dense_acc("dg_fp8_gemm_nt_acc_f32", A, sA, B, sB, C, D, stream)
+
+
+def dg_fp8_gemm_nt_ue8m0_acc_f32(A, sA, B, sB, C, D, stream=None):
+    """As dg_fp8_gemm_nt_acc_f32 with packed UE8M0 scales."""
+    return _dense_acc("dg_fp8_gemm_nt_ue8m0_acc_f32", A, sA, B, sB, C, D, stream)
 
 
 def dg_fp8_gemm_nt_ue8m0(A, sA, B, sB, D, stream=None):

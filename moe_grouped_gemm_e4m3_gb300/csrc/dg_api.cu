@@ -257,14 +257,17 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 //   mode dense: rows = M, G = 1;  contiguous: rows = M_total;  masked: rows = M_max (per group).
 //   sA/sB are FP32 scales, or (block_scaled) packed UE8M0 words: sA [G][ceil(nkb/4)][ldsa] and
 //   sB [G][nnb][ceil(nkb/4)] int32.
+//   C (dense, FP32 D only): D = C + A·Bᵀ. C may be D itself; otherwise it is copied into D first.
 dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, const uint8_t* B, const void* sB,
                    const int32_t* idx, void* D, int rows, int N, int K, int G, cudaStream_t stream,
-                   bool block_scaled = false) {
+                   bool block_scaled = false, const float* C = nullptr, bool accumulate = false) {
   t_last_error.clear();
   if (rows < 0 || N < 0 || K < 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
   if (mode != dg::kDense && G < 1 && rows > 0) {
     if (G == 0) return DG_OK;
   }
+  if (accumulate && (!C || !out_f32 || mode != dg::kDense))
+    return fail(DG_ERR_INVALID_ARG, "the accumulating form needs a C pointer and FP32 D (dense only)");
   if (rows == 0 || N == 0 || G == 0) return DG_OK;
   if (K == 0) return fail(DG_ERR_INVALID_ARG, "K must be positive");
   if (!A || !sA || !B || !sB || !D) return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
@@ -277,6 +280,13 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
     return fail(DG_ERR_ALIGNMENT, "A, B and D must be 16-byte aligned");
   if (!aligned(sA, 4) || !aligned(sB, 4) || (idx && !aligned(idx, 4)))
     return fail(DG_ERR_ALIGNMENT, "sA, sB and index tensors must be 4-byte aligned");
+  if (accumulate) {
+    if (!aligned(C, 16)) return fail(DG_ERR_ALIGNMENT, "C must be 16-byte aligned");
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), d0 = reinterpret_cast<uintptr_t>(D);
+    const uintptr_t bytes = (uintptr_t)rows * (uintptr_t)N * sizeof(float);
+    if (c0 != d0 && c0 < d0 + bytes && d0 < c0 + bytes)
+      return fail(DG_ERR_INVALID_ARG, "C and D overlap without being the same matrix");
+  }
   const long long rows_total = (long long)rows * (mode == dg::kMasked ? G : 1);
   const long long b_rows = (long long)N * (mode == dg::kDense ? 1 : G);
   if (rows_total > INT_MAX - 256 || b_rows > INT_MAX - 256 || K > INT_MAX - 256)
@@ -317,6 +327,11 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.masked_m = mode == dg::kMasked ? idx : nullptr;
   p.D = D;
   p.status = st->status;
+  p.accumulate = accumulate ? 1 : 0;
+  if (accumulate && static_cast<const void*>(C) != D) {
+    cudaError_t ce = cudaMemcpyAsync(D, C, (size_t)rows * N * sizeof(float), cudaMemcpyDeviceToDevice, stream);
+    if (ce != cudaSuccess) return fail_cuda(ce, "cudaMemcpyAsync(C -> D)");
+  }
   if (cfg.splits > 1) {
     const size_t floats = (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n;
     if ((s = ensure_workspace(*st, floats, (size_t)cfg.tiles, stream)) != DG_OK) return s;
@@ -440,6 +455,18 @@ dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, c
                                           dg_stream_t stream) {
   return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream),
                   true);
+}
+
+dg_status dg_fp8_gemm_nt_acc_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, const float* C,
+                                 float* D, int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  C, true);
+}
+
+dg_status dg_fp8_gemm_nt_ue8m0_acc_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                       const float* C, float* D, int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true,
+                  C, true);
 }
 
 int dg_get_tma_aligned_size(int x, int elem_bytes) {

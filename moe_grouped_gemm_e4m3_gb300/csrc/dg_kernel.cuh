@@ -66,6 +66,7 @@ struct GemmParams {
   const uint32_t* sfa;  // packed UE8M0 scales (block-scaled kernel): [G][ceil(nkb/4)][ldsa]
   const uint32_t* sfb;  // packed UE8M0 scales (block-scaled kernel): [G][nnb][ceil(nkb/4)]
   int nkq;              // ceil(nkb / 4): packed scale words along K
+  int accumulate;       // FP32 D only: add the result to D (D = C + A·Bᵀ with D holding C)
   const int32_t* m_indices;
   const int32_t* masked_m;
   void* D;           // row-major, row stride N elements (used by predicated stores)
@@ -625,8 +626,12 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmD, staging + sel * Plan::kStagingBox, n_col0 + chunk * kColsPerBox,
-                         tile.a_row + quad * 32);
+            if (OUT_F32 && p.accumulate)
+              tma_reduce_add_2d(&tmD, staging + sel * Plan::kStagingBox, n_col0 + chunk * kColsPerBox,
+                                tile.a_row + quad * 32);
+            else
+              tma_store_2d(&tmD, staging + sel * Plan::kStagingBox, n_col0 + chunk * kColsPerBox,
+                           tile.a_row + quad * 32);
             tma_store_commit();
           }
           ++store_count;
@@ -638,8 +643,15 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           float* drow = reinterpret_cast<float*>(p.D) + (size_t)d_row * p.N;
 #pragma unroll
           for (int j = 0; j < EPI_COLS; j += 4) {
-            if (n_col0 + j < p.N)
-              *reinterpret_cast<float4*>(drow + n_col0 + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+            if (n_col0 + j < p.N) {
+              float* dst = drow + n_col0 + j;
+              if (p.accumulate) {
+                atomicAdd(dst, acc[j]); atomicAdd(dst + 1, acc[j + 1]);
+                atomicAdd(dst + 2, acc[j + 2]); atomicAdd(dst + 3, acc[j + 3]);
+              } else {
+                *reinterpret_cast<float4*>(dst) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+              }
+            }
           }
         } else {
           uint16_t* drow = reinterpret_cast<uint16_t*>(p.D) + (size_t)d_row * p.N;

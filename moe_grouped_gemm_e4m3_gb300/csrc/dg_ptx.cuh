@@ -126,6 +126,16 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_
                : "memory");
 }
 
+// 2-D tiled reduce-add of a shared-memory box into global memory at (x, y): every element of the
+// box is added to the tensor element it lands on (the tensor map's type, here FP32); elements
+// outside the tensor's bounds are skipped.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* smem_src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until every committed store group has finished reading its shared-memory source.
