@@ -54,6 +54,10 @@ def _load():
         lib.dgo_grouped_masked.argtypes = [P, P, i64, P, P, P, i32, i32, i32, i32, P, P, i32]
         lib.dgo_gemm_nt_sampled.argtypes = [P, P, i64, P, P, i32, i32, i32, i64, P, P, P, i32]
         lib.dgo_gemm_nt_acc.argtypes = [P, P, i64, P, P, P, i32, i32, i32, P, i32]
+        lib.dgo_grouped_masked_swiglu.restype = i32
+        lib.dgo_grouped_masked_swiglu.argtypes = [P, P, i64, P, P, P, i32, i32, i32, i32, P, P, i32]
+        lib.dgo_silu.restype = ctypes.c_double
+        lib.dgo_silu.argtypes = [ctypes.c_double]
         lib.dgo_hardware_threads.restype = i32
         lib.dgo_ue8m0_decode.restype = ctypes.c_double
         lib.dgo_ue8m0_decode.argtypes = [ctypes.c_uint8]
@@ -165,6 +169,36 @@ def grouped_masked(A, sA, B, sB, masked_m, ref64_init=None, D_init=None, threads
     bad = _load().dgo_grouped_masked(_p(A), _p(sA), sA.shape[-1], _p(B), _p(sB), _p(masked_m),
                                      G, M_max, N, K, _p(ref), _p(D), _threads(threads))
     return ref, D, int(bad)
+
+
+def silu(x) -> np.ndarray:
+    """x / (1 + e^-x) in FP64."""
+    x = np.asarray(x, np.float64)
+    lib = _load()
+    return np.array([lib.dgo_silu(float(v)) for v in x.ravel()], np.float64).reshape(x.shape)
+
+
+def grouped_masked_swiglu(A, sA, B, sB, masked_m, ref64_init=None, H_init=None, threads=None):
+    """Masked grouped GEMM fused with SwiGLU: B [G, 2I, K] (gate rows then up rows),
+    H[g,m,j] = silu(D[g,m,j])·D[g,m,I+j] for m < masked_m[g]. Returns (ref64, H bf16 bits, n_clamped)."""
+    A, B, sA, sB = _u8(A), _u8(B), _f32(sA), _f32(sB)
+    masked_m = np.ascontiguousarray(masked_m, dtype=np.int32)
+    G, M_max, K = A.shape
+    I = B.shape[1] // 2
+    ref = np.array(ref64_init, np.float64, copy=True) if ref64_init is not None else np.zeros((G, M_max, I), np.float64)
+    H = np.array(H_init, np.uint16, copy=True) if H_init is not None else np.zeros((G, M_max, I), np.uint16)
+    bad = _load().dgo_grouped_masked_swiglu(_p(A), _p(sA), sA.shape[-1], _p(B), _p(sB), _p(masked_m), G, M_max, I,
+                                            K, _p(ref), _p(H), _threads(threads))
+    return ref, H, int(bad)
+
+
+def masked_swiglu_sampled(A, sA, B, sB, gs, ms, js, threads=None) -> np.ndarray:
+    """FP64 values H[g,m,j] of the fused SwiGLU output at sampled positions (rows must be valid)."""
+    I = B.shape[1] // 2
+    js = np.asarray(js, np.int64)
+    gate = masked_sampled(A, sA, B, sB, gs, ms, js, threads)
+    up = masked_sampled(A, sA, B, sB, gs, ms, js + I, threads)
+    return silu(gate) * up
 
 
 def gemm_nt_sampled(A, sA, B, sB, ms, ns, threads=None) -> np.ndarray:

@@ -31,6 +31,12 @@
 //     bits; exponent field 15 with mantissa 7 is NaN; no infinities; largest finite value 448).
 //   * BF16 output rounding: IEEE round-to-nearest-even, taken directly from the FP64 value (no
 //     intermediate FP32 rounding).
+//   * Masked GEMM fused with SwiGLU: the pages' Mega MoE fuses linear 1, SwiGLU and linear 2 of the
+//     experts into one kernel (tr.news.hada.io/topic?id=19459, § "Mega MoE"); this is its first
+//     fusion, on one GPU and with FP8 weights. SwiGLU is taken from its definition (Shazeer, "GLU
+//     Variants Improve Transformer", 2020): silu(gate)·up with silu(x) = x / (1 + e^-x). B holds 2I
+//     rows per group, gate rows [0, I) then up rows [I, 2I) (a reading: the pages give no layout);
+//     H[g,m,j] = silu(D[g,m,j]) · D[g,m,I+j] for the valid rows m < masked_m[g]; other rows untouched.
 //   * Accumulating form D = C + A @ B.T (the kernel naming D = C + A @ B and fp8_gemm_nt's
 //     definition, same page and section): C is an FP32 [M,N] matrix added to the FP64 GEMM value.
 //   * Packed UE8M0 scales (the Blackwell input form): the SM100 implementation takes its scaling
@@ -223,6 +229,40 @@ int dgo_grouped_masked(const uint8_t* A, const float* sA, int64_t ldsa, const ui
   }
   return bad;
 }
+
+// Masked grouped GEMM fused with SwiGLU: A[G,M_max,K], sA[G][nkb][ldsa], B[G,2I,K], sB[G][2I/128][nkb],
+// masked_m[G]; ref64/H [G,M_max,I]. Rows m >= masked_m[g] (clamped to [0, M_max]) are untouched.
+int dgo_grouped_masked_swiglu(const uint8_t* A, const float* sA, int64_t ldsa, const uint8_t* B,
+                              const float* sB, const int32_t* masked_m, int G, int M_max, int I, int K,
+                              double* ref64, uint16_t* H, int threads) {
+  const int nkb = ceil_div(K, 128), N2 = 2 * I, nnb = ceil_div(N2, 128);
+  int bad = 0;
+  for (int g = 0; g < G; ++g) {
+    int valid = masked_m[g];
+    if (valid < 0) { valid = 0; ++bad; }
+    if (valid > M_max) { valid = M_max; ++bad; }
+    const uint8_t* Ag = A + (int64_t)g * M_max * K;
+    const float* sAg = sA + (int64_t)g * nkb * ldsa;
+    const uint8_t* Bg = B + (int64_t)g * N2 * K;
+    const float* sBg = sB + (int64_t)g * nnb * nkb;
+    parallel_rows(valid, threads, [&](int m) {
+      for (int j = 0; j < I; ++j) {
+        const double gate = element(Ag + (int64_t)m * K, sAg + m, ldsa, Bg + (int64_t)j * K,
+                                    sBg + (int64_t)(j / 128) * nkb, K);
+        const int u = I + j;
+        const double up = element(Ag + (int64_t)m * K, sAg + m, ldsa, Bg + (int64_t)u * K,
+                                  sBg + (int64_t)(u / 128) * nkb, K);
+        const double h = gate / (1.0 + std::exp(-gate)) * up;
+        const int64_t o = ((int64_t)g * M_max + m) * I + j;
+        if (ref64) ref64[o] = h;
+        if (H) H[o] = bf16_rne(h);
+      }
+    });
+  }
+  return bad;
+}
+
+double dgo_silu(double x) { return x / (1.0 + std::exp(-x)); }
 
 // Selected elements (ms[i], ns[i]) of a dense problem, in FP64. For a grouped problem the caller
 // passes the group's A/sA/B/sB base pointers.

@@ -11,6 +11,8 @@
   outside the valid region stay untouched.
 * Accumulating form D = C + A·Bᵀ: the hand-worked example with a C added, A = 0 gives C exactly,
   C = 0 gives the plain GEMM bit for bit.
+* Masked GEMM fused with SwiGLU: silu against scipy's logistic function (x·expit(x)) and its limits;
+  the fused output against silu(gate)·up formed from the plain masked oracle's two halves.
 * Packed UE8M0 scales: the OCP MX E8M0 table (golden file) and torch's float8_e8m0fnu conversion
   for all 256 codes; a GEMM with packed scales worked by hand (golden file, pins the byte order
   and both packed layouts); the unpacker against the input generator's independent packer; the
@@ -454,3 +456,38 @@ def test_gemm_acc_reduces_to_its_parts():
     ms, ns = rng.integers(0, M, 100), rng.integers(0, N, 100)
     full = oracle.gemm_nt_acc(a.A, a.sA, b.B[0], b.sB[0], C, threads=2)
     assert np.array_equal(oracle.gemm_nt_acc_sampled(a.A, a.sA, b.B[0], b.sB[0], C, ms, ns), full[ms, ns])
+
+
+# ----------------------------------------------------------------------------------------------
+# Masked GEMM fused with SwiGLU
+
+
+def test_silu_against_scipy_and_limits():
+    from scipy.special import expit
+    x = np.concatenate([np.linspace(-30, 30, 601), [0.0, 1e-8, -1e-8, 700.0, -700.0]])
+    got = oracle.silu(x)
+    want = x * expit(x)
+    assert np.allclose(got, want, rtol=1e-14, atol=1e-300)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    assert oracle.silu(np.array([50.0]))[0] == 50.0
+    assert abs(oracle.silu(np.array([-50.0]))[0]) < 1e-19
+
+
+def test_masked_swiglu_equals_silu_gate_times_up():
+    G, M_max, I, K = 3, 160, 256, 384
+    masked_m = np.array([0, 1, 160], np.int32)
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=15)
+    b = dg_inputs.make_b(G, 2 * I, K, seed=15)
+    H0 = np.full((G, M_max, I), 0xFFFF, np.uint16)
+    ref, H, bad = oracle.grouped_masked_swiglu(a.A, a.sA, b.B, b.sB, masked_m, None, H0, threads=4)
+    assert bad == 0
+    full, _, _ = oracle.grouped_masked(a.A, a.sA, b.B, b.sB, masked_m, threads=4)
+    from scipy.special import expit
+    for g in range(G):
+        v = masked_m[g]
+        gate, up = full[g, :v, :I], full[g, :v, I:]
+        assert np.allclose(ref[g, :v], gate * expit(gate) * up, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+        assert np.all(H[g, v:] == 0xFFFF)
+    assert np.array_equal(H[2], oracle.bf16_from_f64(ref[2]))
+    gs, ms, js = np.array([1, 2, 2]), np.array([0, 5, 159]), np.array([0, 255, 128])
+    assert np.allclose(oracle.masked_swiglu_sampled(a.A, a.sA, b.B, b.sB, gs, ms, js), ref[gs, ms, js], rtol=1e-12)
