@@ -162,6 +162,28 @@ dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, c
                                           int N, int K, dg_stream_t stream);
 
 /*
+ * Masked grouped GEMM fused with SwiGLU (MoE decode): the up/gate projection of each expert and the
+ * SwiGLU after it in one kernel, so the 2I-wide intermediate never reaches memory. It is the first
+ * fusion of the pages' Mega MoE, which fuses linear 1, SwiGLU and linear 2 of the experts
+ * (tr.news.hada.io/topic?id=19459, § "Mega MoE"); here on one GPU with FP8 weights and FP32 scales.
+ *   A  [G,M_max,K] E4M3     sA [G][ceil(K/128)][align4(M_max)]      (as dg_fp8_grouped_masked)
+ *   B  [G,N,K] E4M3 with N = 2I: rows [0, I) are the gate projection, rows [I, 2I) the up projection
+ *      (I a multiple of 128)                                        sB [G][N/128][ceil(K/128)]
+ *   masked_m [G] int32 on the device (as dg_fp8_grouped_masked)
+ *   H  [G,M_max,I] BF16 bits (or FP32 for the _f32 variant):
+ *      H[g,m,j] = silu(D[g,m,j]) · D[g,m,I+j],  D = the masked GEMM,  silu(x) = x / (1 + e^-x)
+ *      (SwiGLU as defined by Shazeer, "GLU Variants Improve Transformer", 2020)
+ *   Rows m >= masked_m[g] of H are never written. The FP32-scale kernel computes D in FP32 and H in FP32
+ *   (expf), then rounds H to BF16 once: H_bf16 == RNE(H_f32).
+ */
+dg_status dg_fp8_grouped_masked_swiglu(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                       const int32_t* masked_m, uint16_t* H, int G, int M_max, int N, int K,
+                                       dg_stream_t stream);
+dg_status dg_fp8_grouped_masked_swiglu_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                           const int32_t* masked_m, float* H, int G, int M_max, int N, int K,
+                                           dg_stream_t stream);
+
+/*
  * Accumulating dense GEMM: D = C + A·Bᵀ, the full definition of fp8_gemm_nt ("DeepGEMM: İnce
  * ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri", tr.news.hada.io/topic?id=19459,
  * § "GEMM arayüzü ve yerleşim kısıtları": the kernels are named after D = C + A @ B, and

@@ -10,6 +10,7 @@ The names mirror the C ABI:
 * ``dg_fp8_grouped_contiguous(A, sA, B, sB, m_indices, D)``  M-grouped, contiguous layout
 * ``dg_fp8_grouped_masked(A, sA, B, sB, masked_m, D)``       M-grouped, masked layout
 * ``*_f32`` variants store the FP32 accumulator instead of BF16 (same kernel and order).
+* ``dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H)``  masked GEMM + SwiGLU: B [G, 2I, K], H [G, M_max, I]
 * ``dg_fp8_gemm_nt_acc_f32(A, sA, B, sB, C, D)``             D = C + A·Bᵀ (FP32 C and D; C may be D)
 * ``*_ue8m0`` variants take power-of-two scales as packed UE8M0 int32 words (four K-groups per
   word, byte j = K-group 4q+j): sA int32 [ceil(ceil(K/128)/4), align4(rows)] (masked: leading G),
@@ -34,7 +35,8 @@ __all__ = [
     "dg_get_num_sms", "dg_get_device_status", "dg_last_error_string", "dg_query_config",
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
-    "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
+    "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
+    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
     "DG_DEV_TIMEOUT",
 ]
@@ -51,6 +53,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
+    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32",
 )
 
 
@@ -84,7 +87,8 @@ def load(build_if_missing: bool = True):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
     for name in ("dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_fp8_grouped_masked_ue8m0",
-                 "dg_fp8_grouped_masked_ue8m0_f32"):
+                 "dg_fp8_grouped_masked_ue8m0_f32", "dg_fp8_grouped_masked_swiglu",
+                 "dg_fp8_grouped_masked_swiglu_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
     lib.dg_get_tma_aligned_size.restype, lib.dg_get_tma_aligned_size.argtypes = i32, [i32, i32]
@@ -236,6 +240,16 @@ def dg_fp8_gemm_nt_acc_f32(A, sA, B, sB, C, D, stream=None):
 def dg_fp8_gemm_nt_ue8m0_acc_f32(A, sA, B, sB, C, D, stream=None):
     """As dg_fp8_gemm_nt_acc_f32 with packed UE8M0 scales."""
     return _dense_acc("dg_fp8_gemm_nt_ue8m0_acc_f32", A, sA, B, sB, C, D, stream)
+
+
+def dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H, stream=None):
+    """Masked grouped GEMM fused with SwiGLU: B [G, 2I, K] (gate rows, then up rows),
+    H [G, M_max, I] = silu(gate)·up over the rows m < masked_m[g]; other rows untouched."""
+    return _masked("dg_fp8_grouped_masked_swiglu", False, A, sA, B, sB, masked_m, H, stream)
+
+
+def dg_fp8_grouped_masked_swiglu_f32(A, sA, B, sB, masked_m, H, stream=None):
+    return _masked("dg_fp8_grouped_masked_swiglu_f32", True, A, sA, B, sB, masked_m, H, stream)
 
 
 def dg_fp8_gemm_nt_ue8m0(A, sA, B, sB, D, stream=None):

@@ -260,7 +260,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 //   C (dense, FP32 D only): D = C + A·Bᵀ. C may be D itself; otherwise it is copied into D first.
 dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, const uint8_t* B, const void* sB,
                    const int32_t* idx, void* D, int rows, int N, int K, int G, cudaStream_t stream,
-                   bool block_scaled = false, const float* C = nullptr, bool accumulate = false) {
+                   bool block_scaled = false, const float* C = nullptr, bool accumulate = false,
+                   bool swiglu = false) {
   t_last_error.clear();
   if (rows < 0 || N < 0 || K < 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
   if (mode != dg::kDense && G < 1 && rows > 0) {
@@ -268,6 +269,10 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   }
   if (accumulate && (!C || !out_f32 || mode != dg::kDense))
     return fail(DG_ERR_INVALID_ARG, "the accumulating form needs a C pointer and FP32 D (dense only)");
+  if (swiglu && (mode != dg::kMasked || block_scaled || accumulate))
+    return fail(DG_ERR_INVALID_ARG, "the fused SwiGLU form is masked, with FP32 scales");
+  if (swiglu && N % 256 != 0)
+    return fail(DG_ERR_ALIGNMENT, "fused SwiGLU: B must hold 2I rows per group with I a multiple of 128");
   if (rows == 0 || N == 0 || G == 0) return DG_OK;
   if (K == 0) return fail(DG_ERR_INVALID_ARG, "K must be positive");
   if (!A || !sA || !B || !sB || !D) return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
@@ -296,7 +301,18 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   dg_status s = device_state(&st);
   if (s != DG_OK) return s;
   const int sms = effective_sms(*st);
-  const Config cfg = choose_config(mode, rows, N, K, mode == dg::kDense ? 1 : G, sms, block_scaled);
+  Config cfg = choose_config(mode, rows, N, K, mode == dg::kDense ? 1 : G, sms, block_scaled);
+  const int d_cols = swiglu ? N / 2 : N;   // width of D (fused SwiGLU: H has I = N/2 columns)
+  if (swiglu) {
+    // one tile = 128 gate rows + 128 up rows of B; no split-K
+    cfg.block_n = 256;
+    cfg.stages = dg::stages_for(256);
+    cfg.splits = 1;
+    cfg.kb_per_split = ceil_div(K, 128);
+    cfg.tiles = ceil_div(rows, 128) * G * (d_cols / 128);
+    cfg.grid = cfg.tiles < sms ? cfg.tiles : sms;
+    if (cfg.grid < 1) cfg.grid = 1;
+  }
   if ((long long)cfg.tiles * cfg.splits > INT_MAX / 2) return fail(DG_ERR_UNSUPPORTED, "too many tiles");
 
   dg::LaunchArgs a;
@@ -310,7 +326,8 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.nnb = ceil_div(N, 128);
   p.ldsa = dg_get_tma_aligned_size(rows, 4);
   p.num_m_blocks = ceil_div(rows, 128);
-  p.num_n_blocks = ceil_div(N, cfg.block_n);
+  p.num_n_blocks = swiglu ? d_cols / 128 : ceil_div(N, cfg.block_n);
+  p.swiglu_i = swiglu ? d_cols : 0;
   p.num_splits = cfg.splits;
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles * cfg.splits;
@@ -343,14 +360,14 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
     return s;
   if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)b_rows, (uint64_t)K, 128,
-                     (uint32_t)cfg.block_n, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
+                     (uint32_t)(swiglu ? 128 : cfg.block_n), CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
     return s;
   if (out_f32) {
-    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)N, (uint64_t)rows_total, (uint64_t)N * 4, 16, 32,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)d_cols, (uint64_t)rows_total,
+                  (uint64_t)d_cols * 4, 16, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
   } else {
-    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)rows_total, (uint64_t)N * 2, 32, 32,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)d_cols, (uint64_t)rows_total,
+                  (uint64_t)d_cols * 2, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
   }
   if (s != DG_OK) return s;
 
@@ -360,11 +377,16 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   a.stream = stream;
   if (print_configs()) {
     static const char* names[3] = {"dense", "contiguous", "masked"};
-    std::fprintf(stderr, "[dg] %s%s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d grid=%d tiles=%d\n",
-                 names[mode], block_scaled ? "/ue8m0" : "", out_f32 ? "/f32" : "", rows, N, K, p.G, cfg.block_n,
-                 cfg.stages, cfg.splits, cfg.grid, cfg.tiles);
+    std::fprintf(stderr, "[dg] %s%s%s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d grid=%d tiles=%d\n",
+                 names[mode], block_scaled ? "/ue8m0" : "", swiglu ? "/swiglu" : "", out_f32 ? "/f32" : "", rows, N, K,
+                 p.G, cfg.block_n, cfg.stages, cfg.splits, cfg.grid, cfg.tiles);
   }
   cudaError_t e;
+  if (swiglu) {
+    e = dg::launch_masked_swiglu(a);
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return DG_OK;
+  }
   if (block_scaled) {
     e = dg::launch_bs(a, static_cast<dg::Mode>(mode));
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
@@ -455,6 +477,20 @@ dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, c
                                           dg_stream_t stream) {
   return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream),
                   true);
+}
+
+dg_status dg_fp8_grouped_masked_swiglu(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                       const int32_t* masked_m, uint16_t* H, int G, int M_max, int N, int K,
+                                       dg_stream_t stream) {
+  return run_gemm(dg::kMasked, false, A, sA, B, sB, masked_m, H, M_max, N, K, G, static_cast<cudaStream_t>(stream),
+                  false, nullptr, false, true);
+}
+
+dg_status dg_fp8_grouped_masked_swiglu_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                           const int32_t* masked_m, float* H, int G, int M_max, int N, int K,
+                                           dg_stream_t stream) {
+  return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, H, M_max, N, K, G, static_cast<cudaStream_t>(stream),
+                  false, nullptr, false, true);
 }
 
 dg_status dg_fp8_gemm_nt_acc_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, const float* C,

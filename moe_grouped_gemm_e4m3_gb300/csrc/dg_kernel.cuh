@@ -67,6 +67,7 @@ struct GemmParams {
   const uint32_t* sfb;  // packed UE8M0 scales (block-scaled kernel): [G][nnb][ceil(nkb/4)]
   int nkq;              // ceil(nkb / 4): packed scale words along K
   int accumulate;       // FP32 D only: add the result to D (D = C + A·Bᵀ with D holding C)
+  int swiglu_i;         // fused SwiGLU: I, the width of H; B holds 2I rows per group (gate, then up)
   const int32_t* m_indices;
   const int32_t* masked_m;
   void* D;           // row-major, row stride N elements (used by predicated stores)
@@ -234,7 +235,7 @@ struct SmemPlan {
   static constexpr uint32_t kStagingPerWarp = 2 * kStagingBox;  // double-buffered
   static constexpr uint32_t kStagingOff = STAGES * kStageBytes;
   static constexpr uint32_t kBarOff = kStagingOff + EPI_WARPS * kStagingPerWarp;
-  static constexpr uint32_t kNumBars = 2 * STAGES + 2 * NBUF + 2;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 2 * NBUF + 2 + 8;   // + fused-SwiGLU hand-over
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kStashOff = kMiscOff + 64;                 // per epilogue warp: its tile
   static constexpr uint32_t kBytes = kStashOff + EPI_WARPS * 64;
@@ -251,6 +252,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
+
+// silu(x) = x / (1 + e^-x), the gate function of SwiGLU.
+__device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
 
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {
@@ -271,7 +279,12 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // load has landed, before the FMAs that consume it. The ring's depth is what hides the round trip
 // "MMA done -> commit -> epilogue loads -> release -> next MMA into that buffer".
 
-template <int BN, int EPI_COLS, int STAGES, int NBUF, Mode MODE, bool OUT_F32>
+//
+// SWIGLU (masked form only, BN = 256): the tile's 256 B rows are 128 gate rows (block n of [0, I))
+// and the 128 up rows I + 128·n ..; the epilogue pairs the two halves and stores
+// H = silu(gate)·up, 128 columns of the [G·M_max, I] output per tile.
+
+template <int BN, int EPI_COLS, int STAGES, int NBUF, Mode MODE, bool OUT_F32, bool SWIGLU>
 __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
@@ -283,6 +296,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocation: power of two");
   constexpr uint32_t kIdesc = make_idesc_e4m3_f32(128, BN);
   static_assert(kChunks % 2 == 0, "TMEM loads go in pairs");
+  static_assert(!SWIGLU || (BN == 256 && EPI_COLS == 128 && MODE == kMasked), "fused SwiGLU: masked, BN = 256");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -292,6 +306,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   uint64_t* tempty_bar = tfull_bar + NBUF;         // [buffer]: every epilogue warp has loaded it
   uint64_t* epi_arrive_bar = tempty_bar + NBUF;       // split-K: all epilogue warps published a partial
   uint64_t* epi_release_bar = epi_arrive_bar + 1;  // split-K: the arrival count has been taken
+  uint64_t* xfull_bar = epi_release_bar + 1;       // fused SwiGLU [quadrant]: up values are in the buffer
+  uint64_t* xempty_bar = xfull_bar + 4;            // fused SwiGLU [quadrant]: the gate warp has read them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Plan::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 8);
@@ -310,6 +326,10 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     }
     mbar_init(epi_arrive_bar, kEpiWarps);
     mbar_init(epi_release_bar, 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&xfull_bar[q], 1);
+      mbar_init(&xempty_bar[q], 1);
+    }
     *abort_flag = 0;
     *last_flag = 0;
     fence_barrier_init();
@@ -359,7 +379,15 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             uint8_t* sa = smem + s * Plan::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
             tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
-            tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
+            if constexpr (SWIGLU) {
+              // gate rows 128·n .. and up rows I + 128·n .. (B's tensor map box is 128 rows)
+              const int gate_row = tile.g * p.N + tile.n_blk * 128;
+              tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, gate_row, policy);
+              tma_load_2d(&tmB, sa + Plan::kABytes + 128 * 128, &full_bar[s], kb * 128, gate_row + p.swiglu_i,
+                          policy);
+            } else {
+              tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
+            }
             issued_phase[s] = (int)ph;
           }
         }
@@ -436,7 +464,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     const int row_in_tile = quad * 32 + lane;
     uint8_t* staging = smem + Plan::kStagingOff + warp * Plan::kStagingPerWarp;
     const uint32_t staging_addr = smem_u32(staging);
-    uint32_t acc_it = 0, sk_it = 0;
+    uint32_t acc_it = 0, sk_it = 0, x_it = 0;
     bool alive = true;
     uint32_t store_count = 0;   // TMA store boxes issued by this warp
     // Tile columns EPI_COLS*cgrp + i, as FP32 pairs so that each promotion step is one packed
@@ -463,7 +491,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       const int m_local = tile.m_blk * 128 + row_in_tile;   // row within the group
       const bool row_exists = row_in_tile < tile.rows;
       const float* sa_ptr = p.sA + (MODE == kMasked ? (size_t)tile.g * p.nkb * p.ldsa : 0) + m_local;
-      const int n_col0 = tile.n_blk * BN + cgrp * EPI_COLS;  // first column of this warp
+      // first column of this warp (as a row of B: fused SwiGLU puts the up rows at I + 128·n)
+      const int n_col0 = SWIGLU ? (cgrp ? p.swiglu_i : 0) + tile.n_blk * 128 : tile.n_blk * BN + cgrp * EPI_COLS;
       const bool col_exists = n_col0 < p.N;
       const float* sb_ptr = p.sB + ((size_t)tile.g * p.nnb + (col_exists ? n_col0 / 128 : 0)) * p.nkb;
       // Warps with no row or no column in range only keep the TMEM handshake going.
@@ -575,6 +604,107 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             }
           }
         }
+      }
+
+      if constexpr (SWIGLU) {
+        // Fused SwiGLU: warp cgrp 1 (up) hands its accumulators to warp cgrp 0 (gate) of the same
+        // quadrant, 32 columns per round, through its own staging buffer; both warps hold the same
+        // 32 rows. The hand-over is guarded by two mbarriers per quadrant (bounded waits). The gate
+        // warp forms silu(gate)·up and stores those 32 columns of H.
+        const unsigned row_mask = __ballot_sync(0xffffffffu, row_exists);
+        if (row_mask == 0u) continue;                   // the same decision in both warps of the pair
+        const bool all_rows = row_mask == 0xffffffffu;
+        const uint32_t xchg = smem_u32(smem + Plan::kStagingOff + (quad + 4) * Plan::kStagingPerWarp);
+        const int h_col0 = tile.n_blk * 128;           // the tile's first column of H
+        constexpr int kColsPerBox = OUT_F32 ? 16 : 32;
+        bool ok = true;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {   // unrolled: the accumulator indices stay compile-time constants
+          const uint32_t xph = x_it & 1;
+          ++x_it;
+          if (cgrp == 1) {
+            ok = mbar_wait(&xempty_bar[quad], xph ^ 1, abort_flag, p.status);
+            if (!ok) break;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int c = r * 32 + j * 4;
+              st_shared_v4(xchg + lane * 128 + (uint32_t)((j ^ (lane & 7)) * 16), __float_as_uint(acc[c]),
+                           __float_as_uint(acc[c + 1]), __float_as_uint(acc[c + 2]), __float_as_uint(acc[c + 3]));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xfull_bar[quad]);
+            continue;
+          }
+          ok = mbar_wait(&xfull_bar[quad], xph, abort_flag, p.status);
+          if (!ok) break;
+          float h[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t u0, u1, u2, u3;
+            ld_shared_v4(xchg + lane * 128 + (uint32_t)((j ^ (lane & 7)) * 16), u0, u1, u2, u3);
+            const int c = r * 32 + j * 4;
+            h[j * 4 + 0] = silu_f32(acc[c + 0]) * __uint_as_float(u0);
+            h[j * 4 + 1] = silu_f32(acc[c + 1]) * __uint_as_float(u1);
+            h[j * 4 + 2] = silu_f32(acc[c + 2]) * __uint_as_float(u2);
+            h[j * 4 + 3] = silu_f32(acc[c + 3]) * __uint_as_float(u3);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&xempty_bar[quad]);   // the up warp may refill the buffer
+          if (all_rows) {
+#pragma unroll
+            for (int box = 0; box < 32 / kColsPerBox; ++box) {
+              const uint32_t sel = store_count & 1;
+              if (store_count >= 2) {
+                if (lane == 0) tma_store_wait_read_1();
+                __syncwarp();
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {   // four 16-byte pieces per 64-byte row
+                uint32_t w0, w1, w2, w3;
+                if constexpr (OUT_F32) {
+                  const int c = box * 16 + j * 4;
+                  w0 = __float_as_uint(h[c]); w1 = __float_as_uint(h[c + 1]);
+                  w2 = __float_as_uint(h[c + 2]); w3 = __float_as_uint(h[c + 3]);
+                } else {
+                  const int c = j * 8;
+                  w0 = pack_bf16x2(h[c], h[c + 1]); w1 = pack_bf16x2(h[c + 2], h[c + 3]);
+                  w2 = pack_bf16x2(h[c + 4], h[c + 5]); w3 = pack_bf16x2(h[c + 6], h[c + 7]);
+                }
+                const uint32_t phys = (uint32_t)(j ^ ((lane >> 1) & 3));
+                st_shared_v4(staging_addr + sel * Plan::kStagingBox + lane * 64 + phys * 16, w0, w1, w2, w3);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmD, staging + sel * Plan::kStagingBox, h_col0 + r * 32 + box * kColsPerBox,
+                             tile.a_row + quad * 32);
+                tma_store_commit();
+              }
+              ++store_count;
+              __syncwarp();
+            }
+          } else if (row_exists) {
+            // predicated plain stores: rows past masked_m stay untouched
+            const size_t hrow = (size_t)(tile.a_row + row_in_tile) * p.swiglu_i + h_col0 + r * 32;
+            if constexpr (OUT_F32) {
+              float* dst = reinterpret_cast<float*>(p.D) + hrow;
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(dst + j) = make_float4(h[j], h[j + 1], h[j + 2], h[j + 3]);
+            } else {
+              uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + hrow;
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(h[j], h[j + 1]); v.y = pack_bf16x2(h[j + 2], h[j + 3]);
+                v.z = pack_bf16x2(h[j + 4], h[j + 5]); v.w = pack_bf16x2(h[j + 6], h[j + 7]);
+                *reinterpret_cast<uint4*>(dst + j) = v;
+              }
+            }
+          }
+        }
+        if (!ok) { alive = false; break; }
+        continue;
       }
 
       // ---------------- output

@@ -32,18 +32,20 @@ constexpr int tmem_bufs_for(int block_n) { return 512 / block_n; }
 cudaError_t launch_dense(const LaunchArgs& a);
 cudaError_t launch_contiguous(const LaunchArgs& a);
 cudaError_t launch_masked(const LaunchArgs& a);
+// The masked form fused with SwiGLU (block_n 256, FP32-scale kernel).
+cudaError_t launch_masked_swiglu(const LaunchArgs& a);
 // The block-scaled kernel for packed UE8M0 scales (block_n is always 256).
 cudaError_t launch_bs(const LaunchArgs& a, Mode mode);
 
 // Launches one instantiation; sets its dynamic shared-memory limit on first use per device.
-template <int BN, Mode MODE, bool OUT_F32>
+template <int BN, Mode MODE, bool OUT_F32, bool SWIGLU = false>
 cudaError_t launch_instance(const LaunchArgs& a) {
   constexpr int STAGES = stages_for(BN);
   constexpr int EPI_COLS = epi_cols_for(BN);
   constexpr int NBUF = tmem_bufs_for(BN);
   using R = Roles<BN, EPI_COLS>;
   using Plan = SmemPlan<BN, STAGES, R::kEpiWarps, NBUF>;
-  auto kernel = fp8_gemm_kernel<BN, EPI_COLS, STAGES, NBUF, MODE, OUT_F32>;
+  auto kernel = fp8_gemm_kernel<BN, EPI_COLS, STAGES, NBUF, MODE, OUT_F32, SWIGLU>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
