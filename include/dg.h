@@ -162,6 +162,34 @@ dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, c
                                           int N, int K, dg_stream_t stream);
 
 /*
+ * Dense GEMM in the other layouts. The SM100 implementation supports the NT, TN, NN and TT layouts
+ * (fp8_gemm_{nt, nn, tn, tt}: "DeepGEMM: İnce ölçeklendirmeyle temiz ve verimli FP8 GEMM
+ * çekirdekleri", tr.news.hada.io/topic?id=19459, § "GEMM arayüzü ve yerleşim kısıtları" and
+ * § "Dense ve Grouped GEMM"). The product is always D[M,N] = A·Bᵀ of the logical A[M,K] and B[N,K];
+ * the letters say how A and B are stored:
+ *   nt (dg_fp8_gemm_nt): A [M,K], B [N,K]  (both K-contiguous)
+ *   nn:                  A [M,K], B [K,N]  (B N-contiguous)
+ *   tn:                  A [K,M], B [K,N]  (both M/N-contiguous: e.g. weight gradients over tokens)
+ *   tt:                  A [K,M], B [N,K]
+ * The scales keep the logical granularity and layouts of dg_fp8_gemm_nt: sA [ceil(K/128)][align4(M)]
+ * (one per 1x128 K-group of each logical row of A), sB [ceil(N/128)][ceil(K/128)]. A stored [K,M]
+ * needs M % 16 == 0; B stored [K,N] needs N % 16 == 0 (16-byte TMA strides). The tensor core reads
+ * the M/N-contiguous tiles directly (no transposition pass). Other conventions as dg_fp8_gemm_nt.
+ */
+dg_status dg_fp8_gemm_nn(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D,
+                         int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_nn_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D,
+                             int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_tn(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D,
+                         int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_tn_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D,
+                             int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_tt(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D,
+                         int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_tt_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D,
+                             int M, int N, int K, dg_stream_t stream);
+
+/*
  * Masked grouped GEMM fused with SwiGLU (MoE decode): the up/gate projection of each expert and the
  * SwiGLU after it in one kernel, so the 2I-wide intermediate never reaches memory. It is the first
  * fusion of the pages' Mega MoE, which fuses linear 1, SwiGLU and linear 2 of the experts

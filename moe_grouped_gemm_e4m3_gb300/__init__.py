@@ -10,6 +10,8 @@ The names mirror the C ABI:
 * ``dg_fp8_grouped_contiguous(A, sA, B, sB, m_indices, D)``  M-grouped, contiguous layout
 * ``dg_fp8_grouped_masked(A, sA, B, sB, masked_m, D)``       M-grouped, masked layout
 * ``*_f32`` variants store the FP32 accumulator instead of BF16 (same kernel and order).
+* ``dg_fp8_gemm_{nn,tn,tt}(A, sA, B, sB, D, M=, N=, K=)``     dense D = A·Bᵀ with A stored [K,M] (t) and/or
+  B stored [K,N] (second letter n); the scales keep dg_fp8_gemm_nt's layouts
 * ``dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H)``  masked GEMM + SwiGLU: B [G, 2I, K], H [G, M_max, I]
 * ``dg_fp8_gemm_nt_acc_f32(A, sA, B, sB, C, D)``             D = C + A·Bᵀ (FP32 C and D; C may be D)
 * ``*_ue8m0`` variants take power-of-two scales as packed UE8M0 int32 words (four K-groups per
@@ -36,7 +38,8 @@ __all__ = [
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
-    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
+    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
+    "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
     "DG_DEV_TIMEOUT",
 ]
@@ -53,7 +56,8 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
-    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32",
+    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
+    "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
 )
 
 
@@ -79,7 +83,8 @@ def load(build_if_missing: bool = True):
     lib = ctypes.CDLL(path)
     P, i32 = ctypes.c_void_p, ctypes.c_int
     for name in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nt_noalloc", "dg_fp8_gemm_nt_ue8m0",
-                 "dg_fp8_gemm_nt_ue8m0_f32"):
+                 "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32", "dg_fp8_gemm_tn",
+                 "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, i32, i32, i32, P]
     for name in ("dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32", "dg_fp8_grouped_contiguous_ue8m0",
@@ -240,6 +245,40 @@ def dg_fp8_gemm_nt_acc_f32(A, sA, B, sB, C, D, stream=None):
 def dg_fp8_gemm_nt_ue8m0_acc_f32(A, sA, B, sB, C, D, stream=None):
     """As dg_fp8_gemm_nt_acc_f32 with packed UE8M0 scales."""
     return _dense_acc("dg_fp8_gemm_nt_ue8m0_acc_f32", A, sA, B, sB, C, D, stream)
+
+
+def _dense_layout(name, f32, A, sA, B, sB, D, M, N, K, stream):
+    lib = load()
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", _f32()), _ptr(D, "D", _d_types(f32)), M, N, K, _stream(stream)))
+    return D
+
+
+def dg_fp8_gemm_nn(A, sA, B, sB, D, M, N, K, stream=None):
+    """D[M,N] = A·Bᵀ with A stored [M,K] and B stored [K,N] (N contiguous)."""
+    return _dense_layout("dg_fp8_gemm_nn", False, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_nn_f32(A, sA, B, sB, D, M, N, K, stream=None):
+    return _dense_layout("dg_fp8_gemm_nn_f32", True, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_tn(A, sA, B, sB, D, M, N, K, stream=None):
+    """D[M,N] = A·Bᵀ with A stored [K,M] and B stored [K,N] (both M/N contiguous)."""
+    return _dense_layout("dg_fp8_gemm_tn", False, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_tn_f32(A, sA, B, sB, D, M, N, K, stream=None):
+    return _dense_layout("dg_fp8_gemm_tn_f32", True, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_tt(A, sA, B, sB, D, M, N, K, stream=None):
+    """D[M,N] = A·Bᵀ with A stored [K,M] and B stored [N,K]."""
+    return _dense_layout("dg_fp8_gemm_tt", False, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_tt_f32(A, sA, B, sB, D, M, N, K, stream=None):
+    return _dense_layout("dg_fp8_gemm_tt_f32", True, A, sA, B, sB, D, M, N, K, stream)
 
 
 def dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H, stream=None):

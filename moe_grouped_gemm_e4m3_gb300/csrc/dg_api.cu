@@ -261,7 +261,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, const uint8_t* B, const void* sB,
                    const int32_t* idx, void* D, int rows, int N, int K, int G, cudaStream_t stream,
                    bool block_scaled = false, const float* C = nullptr, bool accumulate = false,
-                   bool swiglu = false) {
+                   bool swiglu = false, bool a_mn = false, bool b_mn = false) {
   t_last_error.clear();
   if (rows < 0 || N < 0 || K < 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
   if (mode != dg::kDense && G < 1 && rows > 0) {
@@ -273,9 +273,13 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
     return fail(DG_ERR_INVALID_ARG, "the fused SwiGLU form is masked, with FP32 scales");
   if (swiglu && N % 256 != 0)
     return fail(DG_ERR_ALIGNMENT, "fused SwiGLU: B must hold 2I rows per group with I a multiple of 128");
+  if ((a_mn || b_mn) && (mode != dg::kDense || block_scaled))
+    return fail(DG_ERR_INVALID_ARG, "the NN/TN/TT layouts are dense, with FP32 scales");
   if (rows == 0 || N == 0 || G == 0) return DG_OK;
   if (K == 0) return fail(DG_ERR_INVALID_ARG, "K must be positive");
   if (!A || !sA || !B || !sB || !D) return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
+  if (a_mn && rows % 16 != 0) return fail(DG_ERR_ALIGNMENT, "A stored [K,M]: M must be a multiple of 16");
+  if (b_mn && N % 16 != 0) return fail(DG_ERR_ALIGNMENT, "B stored [K,N]: N must be a multiple of 16");
   if (mode != dg::kDense && !idx) return fail(DG_ERR_INVALID_ARG, mode == dg::kMasked ? "null masked_m" : "null m_indices");
   if (K % 16 != 0) return fail(DG_ERR_ALIGNMENT, "K must be a multiple of 16 (16-byte rows of E4M3 A and B)");
   if (N % (out_f32 ? 4 : 8) != 0)
@@ -328,6 +332,8 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.num_m_blocks = ceil_div(rows, 128);
   p.num_n_blocks = swiglu ? d_cols / 128 : ceil_div(N, cfg.block_n);
   p.swiglu_i = swiglu ? d_cols : 0;
+  p.a_mn = a_mn ? 1 : 0;
+  p.b_mn = b_mn ? 1 : 0;
   p.num_splits = cfg.splits;
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles * cfg.splits;
@@ -356,12 +362,22 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
     p.counters = st->counters;
   }
 
-  if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)K, (uint64_t)rows_total, (uint64_t)K, 128, 128,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
+  if (a_mn) {   // A stored [K, M]: M contiguous
+    if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)rows_total, (uint64_t)K, (uint64_t)rows_total,
+                       128, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
+      return s;
+  } else if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)K, (uint64_t)rows_total, (uint64_t)K,
+                            128, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK) {
     return s;
-  if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)b_rows, (uint64_t)K, 128,
-                     (uint32_t)(swiglu ? 128 : cfg.block_n), CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
+  }
+  if (b_mn) {   // B stored [K, N]: N contiguous, boxes of 128 N-bytes x 128 K-rows
+    if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)b_rows, (uint64_t)K, (uint64_t)b_rows, 128,
+                       128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
+      return s;
+  } else if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)b_rows, (uint64_t)K, 128,
+                            (uint32_t)(swiglu ? 128 : cfg.block_n), CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK) {
     return s;
+  }
   if (out_f32) {
     s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)d_cols, (uint64_t)rows_total,
                   (uint64_t)d_cols * 4, 16, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
@@ -477,6 +493,42 @@ dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, c
                                           dg_stream_t stream) {
   return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream),
                   true);
+}
+
+dg_status dg_fp8_gemm_nn(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int M,
+                         int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  nullptr, false, false, false, true);
+}
+
+dg_status dg_fp8_gemm_nn_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D, int M,
+                             int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  nullptr, false, false, false, true);
+}
+
+dg_status dg_fp8_gemm_tn(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int M,
+                         int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  nullptr, false, false, true, true);
+}
+
+dg_status dg_fp8_gemm_tn_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D, int M,
+                             int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  nullptr, false, false, true, true);
+}
+
+dg_status dg_fp8_gemm_tt(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int M,
+                         int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  nullptr, false, false, true, false);
+}
+
+dg_status dg_fp8_gemm_tt_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D, int M,
+                             int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  nullptr, false, false, true, false);
 }
 
 dg_status dg_fp8_grouped_masked_swiglu(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,

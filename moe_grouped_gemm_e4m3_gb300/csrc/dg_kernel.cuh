@@ -68,6 +68,7 @@ struct GemmParams {
   int nkq;              // ceil(nkb / 4): packed scale words along K
   int accumulate;       // FP32 D only: add the result to D (D = C + A·Bᵀ with D holding C)
   int swiglu_i;         // fused SwiGLU: I, the width of H; B holds 2I rows per group (gate, then up)
+  int a_mn, b_mn;       // dense layouts: A stored [K,M] / B stored [K,N] (MN-major) instead of K-major
   const int32_t* m_indices;
   const int32_t* masked_m;
   void* D;           // row-major, row stride N elements (used by predicated stores)
@@ -378,8 +379,16 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             if (!ok) break;
             uint8_t* sa = smem + s * Plan::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
-            tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
-            if constexpr (SWIGLU) {
+            if (p.a_mn)   // A stored [K, M]: the box is 128 K-rows x 128 M-bytes
+              tma_load_2d(&tmA, sa, &full_bar[s], tile.a_row, kb * 128, policy);
+            else
+              tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
+            if (p.b_mn) {  // B stored [K, N]: BN/128 boxes of 128 K-rows x 128 N-bytes, 16 KB apart
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
+                tma_load_2d(&tmB, sa + Plan::kABytes + h * 128 * 128, &full_bar[s], b_row + h * 128, kb * 128,
+                            policy);
+            } else if constexpr (SWIGLU) {
               // gate rows 128·n .. and up rows I + 128·n .. (B's tensor map box is 128 rows)
               const int gate_row = tile.g * p.N + tile.n_blk * 128;
               tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, gate_row, policy);
@@ -426,13 +435,17 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
-            const uint64_t adesc = make_sw128_kmajor_desc(a_addr);
-            const uint64_t bdesc = make_sw128_kmajor_desc(a_addr + Plan::kABytes);
+            const uint64_t adesc = p.a_mn ? make_sw128_mnmajor_desc(a_addr, 128 * 128) : make_sw128_kmajor_desc(a_addr);
+            const uint64_t bdesc = p.b_mn ? make_sw128_mnmajor_desc(a_addr + Plan::kABytes, 128 * 128)
+                                          : make_sw128_kmajor_desc(a_addr + Plan::kABytes);
+            // one K=32 step: +32 bytes inside a K-major 128-byte row (+2 in the >>4 address field), or
+            // +32 rows of 128 bytes in an MN-major tile (+256)
+            const uint32_t a_step = p.a_mn ? 256u : 2u, b_step = p.b_mn ? 256u : 2u;
+            const uint32_t idesc = kIdesc | ((uint32_t)p.a_mn << 15) | ((uint32_t)p.b_mn << 16);
             const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field
-              mma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+              mma_e4m3(d_tmem, adesc + a_step * k, bdesc + b_step * k, idesc, k > 0 ? 1u : 0u);
             }
             mma_commit(&empty_bar[s]);
             mma_commit(&tfull_bar[b]);

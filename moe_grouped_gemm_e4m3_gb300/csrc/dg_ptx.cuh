@@ -205,6 +205,21 @@ __device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile stored with the 128-byte swizzle, as a
+// TMA box of 128 K-rows x 128 bytes (M or N) writes it: 8-row swizzle atoms along K 1024 bytes apart
+// (stride byte offset) and `atom_stride` bytes between 128-byte-wide atoms along M/N (leading byte
+// offset; unused when the tile is one atom wide). One K=32 step advances the start by 32 rows = 4096
+// bytes. (Layout measured on GB300 against exact integer products.)
+__device__ __forceinline__ uint64_t make_sw128_mnmajor_desc(uint32_t smem_addr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((atom_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B, FP32 accumulator, both K-major,
 // shape M x N: D format [4,6) = 1 (F32), A format [7,10) = 0 (E4M3), B format [10,13) = 0 (E4M3),
 // A/B major bits 15/16 = 0 (K-major), N >> 3 at [17,23), M >> 4 at [24,29).
