@@ -638,6 +638,51 @@ def run_all_configs(args):
                dict(scales, cfg=query_config(dg, 2, M_max, N, K, G)))
     for (M, N, K) in ((4096, 2112, 7168), (4096, 576, 7168), (4096, 7168, 32768)):
         dense("5 stress (Student-t, outliers)", M, N, K, dist=dg_inputs.STUDENT_T3, outliers=0.01)
+    # the masked form fused with SwiGLU (FP32 scales only): B holds 2I rows, H has I columns
+    if not UE8M0:
+        for (N2, K) in ((4096, 7168),):
+            G, M_max, I = 16, 256, N2 // 2
+            mm = dg_inputs.make_masked_m(G, M_max, seed=0)
+            a = dg_inputs.make_masked_a(G, M_max, K, seed=0)
+            b = dg_inputs.make_b(G, N2, K, seed=0)
+            A, sA, B, sB, MM = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(mm)
+            H = torch.empty(G, M_max, I, dtype=torch.bfloat16, device="cuda")
+            ms = timeit(lambda: dg.dg_fp8_grouped_masked_swiglu(A, sA, B, sB, MM, H))
+            valid = int(mm.sum())
+            nkb = -(-K // 128)
+            active = int((mm > 0).sum())
+            nbytes = valid * K + active * N2 * K + 4 * valid * nkb + 4 * G * (N2 // 128) * nkb + 2 * valid * I
+            report("7 masked + SwiGLU (fused)", f"G=16 M_max=256 sum(masked_m)={valid} 2I={N2} K={K}",
+                   2.0 * valid * N2 * K, nbytes, ms, dict(scales))
+            del A, B, H
+    # the NN / TN / TT layouts (FP32 scales only): A stored [K,M] and/or B stored [K,N]
+    if not UE8M0:
+        M, N, K = 4096, 7168, 2048
+        a = dg_inputs.make_a(M, K, seed=0)
+        b = dg_inputs.make_b(1, N, K, seed=0)
+        for layout, (a_t, b_t) in (("nn", (False, True)), ("tn", (True, True)), ("tt", (True, False))):
+            A = dev(np.ascontiguousarray(a.A.T) if a_t else a.A)
+            B = dev(np.ascontiguousarray(b.B[0].T) if b_t else b.B[0])
+            sA, sB = dev(a.sA), dev(b.sB[0])
+            D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            fn = getattr(dg, f"dg_fp8_gemm_{layout}")
+            ms = timeit(lambda: fn(A, sA, B, sB, D, M, N, K))
+            report(f"8 layout {layout}", f"{M}x{N}x{K}", 2.0 * M * N * K, algorithmic_bytes(M, N, K), ms,
+                   dict(scales, cfg=query_config(dg, 0, M, N, K)))
+            del A, B, D
+    # the accumulating form D = C + A·Bᵀ (FP32 C = D, in place): C is read and D written in FP32
+    for (M, N, K) in ((4096, 7168, 16384), (4096, 7168, 2048)):
+        a = dg_inputs.make_a(M, K, seed=0, ue8m0=UE8M0)
+        b = dg_inputs.make_b(1, N, K, seed=0, ue8m0=UE8M0)
+        gsA, gsB = gpu_scales(a, b)
+        A, sA, B, sB = dev(a.A), dev(gsA), dev(b.B[0]), dev(gsB[0])
+        D = torch.zeros(M, N, dtype=torch.float32, device="cuda")
+        acc = dg.dg_fp8_gemm_nt_ue8m0_acc_f32 if UE8M0 else dg.dg_fp8_gemm_nt_acc_f32
+        ms = timeit(lambda: acc(A, sA, B, sB, D, D))
+        nbytes = algorithmic_bytes(M, N, K) - 2 * M * N + 8 * M * N
+        report("6 accumulate D = C + A·Bᵀ (FP32, in place)", f"{M}x{N}x{K}", 2.0 * M * N * K, nbytes, ms,
+               dict(scales, cfg=query_config(dg, 0, M, N, K)))
+        del A, B, D
 
 
 def main():
