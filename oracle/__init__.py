@@ -56,6 +56,8 @@ def _load():
         lib.dgo_gemm_nt_acc.argtypes = [P, P, i64, P, P, P, i32, i32, i32, P, i32]
         lib.dgo_grouped_masked_swiglu.restype = i32
         lib.dgo_grouped_masked_swiglu.argtypes = [P, P, i64, P, P, P, i32, i32, i32, i32, P, P, i32]
+        lib.dgo_k_grouped.restype = i32
+        lib.dgo_k_grouped.argtypes = [P, P, i64, P, P, P, i32, i32, i32, i32, P, i32]
         lib.dgo_silu.restype = ctypes.c_double
         lib.dgo_silu.argtypes = [ctypes.c_double]
         lib.dgo_hardware_threads.restype = i32
@@ -199,6 +201,24 @@ def masked_swiglu_sampled(A, sA, B, sB, gs, ms, js, threads=None) -> np.ndarray:
     gate = masked_sampled(A, sA, B, sB, gs, ms, js, threads)
     up = masked_sampled(A, sA, B, sB, gs, ms, js + I, threads)
     return silu(gate) * up
+
+
+def k_grouped(A, sA, B, sB, offsets, threads=None) -> np.ndarray:
+    """K-grouped D[g] = Σ_{k in [off[g], off[g+1])} of the logical A[M,K_total]·B[N,K_total]ᵀ terms,
+    with the scales of those K-blocks. Returns ref64 [G,M,N]."""
+    A, B, sA, sB = _u8(A), _u8(B), _f32(sA), _f32(sB)
+    if B.ndim == 3:
+        B, sB = B[0], sB[0]
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    M, K = A.shape
+    N = B.shape[0]
+    G = len(off) - 1
+    ref = np.zeros((G, M, N), np.float64)
+    bad = _load().dgo_k_grouped(_p(A), _p(sA), sA.shape[-1], _p(B), _p(sB), _p(off), G, M, N, K, _p(ref),
+                                _threads(threads))
+    if bad:
+        raise ValueError(f"{bad} invalid K offsets")
+    return ref
 
 
 def gemm_nt_sampled(A, sA, B, sB, ms, ns, threads=None) -> np.ndarray:

@@ -37,6 +37,11 @@
 //     Variants Improve Transformer", 2020): silu(gate)·up with silu(x) = x / (1 + e^-x). B holds 2I
 //     rows per group, gate rows [0, I) then up rows [I, 2I) (a reading: the pages give no layout);
 //     H[g,m,j] = silu(D[g,m,j]) · D[g,m,I+j] for the valid rows m < masked_m[g]; other rows untouched.
+//   * K-grouped contiguous GEMM (MoE weight backward: k_grouped_fp8_gemm_tn_contiguous, grouped
+//     along K with M and N fixed, same page, § "Dense ve Grouped GEMM"): the experts' token
+//     segments are concatenated along K, each a multiple of 128 long; group g covers
+//     k in [off[g], off[g+1]) and D[g] = Σ over that range, with the scales of those K-blocks.
+//     An empty segment gives D[g] = 0.
 //   * Accumulating form D = C + A @ B.T (the kernel naming D = C + A @ B and fp8_gemm_nt's
 //     definition, same page and section): C is an FP32 [M,N] matrix added to the FP64 GEMM value.
 //   * Packed UE8M0 scales (the Blackwell input form): the SM100 implementation takes its scaling
@@ -121,6 +126,20 @@ double element(const uint8_t* a_row, const float* sA_m, int64_t ldsa,
     for (int k = k0; k < k1; ++k) P += e4m3_value(a_row[k]) * e4m3_value(b_row[k]);
     const double scale = (double)sA_m[(int64_t)kb * ldsa] * (double)sB_n[kb];
     acc += scale * P;
+  }
+  return acc;
+}
+
+// As element(), over the K-blocks [kb0, kb1) only (the rows are indexed from k = 0).
+double element_range(const uint8_t* a_row, const float* sA_m, int64_t ldsa, const uint8_t* b_row,
+                     const float* sB_n, int K, int kb0, int kb1) {
+  double acc = 0.0;
+  for (int kb = kb0; kb < kb1; ++kb) {
+    const int k0 = kb * 128;
+    const int k1 = (k0 + 128 < K) ? k0 + 128 : K;
+    double P = 0.0;
+    for (int k = k0; k < k1; ++k) P += e4m3_value(a_row[k]) * e4m3_value(b_row[k]);
+    acc += (double)sA_m[(int64_t)kb * ldsa] * (double)sB_n[kb] * P;
   }
   return acc;
 }
@@ -263,6 +282,28 @@ int dgo_grouped_masked_swiglu(const uint8_t* A, const float* sA, int64_t ldsa, c
 }
 
 double dgo_silu(double x) { return x / (1.0 + std::exp(-x)); }
+
+// K-grouped: logical A[M,K_total] and B[N,K_total] (K contiguous), sA[nkb][ldsa], sB[nnb][nkb] over the
+// whole K_total, off[G+1] K offsets (multiples of 128, non-decreasing); ref64 [G,M,N]. Returns the
+// number of invalid offsets (not a multiple of 128, decreasing, or beyond K_total); then computes nothing.
+int dgo_k_grouped(const uint8_t* A, const float* sA, int64_t ldsa, const uint8_t* B, const float* sB,
+                  const int32_t* off, int G, int M, int N, int K_total, double* ref64, int threads) {
+  int bad = 0;
+  for (int g = 0; g <= G; ++g)
+    if (off[g] % 128 != 0 || off[g] < 0 || off[g] > K_total || (g > 0 && off[g] < off[g - 1])) ++bad;
+  if (bad) return bad;
+  const int nkb = ceil_div(K_total, 128);
+  for (int g = 0; g < G; ++g) {
+    const int kb0 = off[g] / 128, kb1 = off[g + 1] / 128;
+    parallel_rows(M, threads, [&](int m) {
+      for (int n = 0; n < N; ++n)
+        ref64[((int64_t)g * M + m) * N + n] =
+            element_range(A + (int64_t)m * K_total, sA + m, ldsa, B + (int64_t)n * K_total,
+                          sB + (int64_t)(n / 128) * nkb, K_total, kb0, kb1);
+    });
+  }
+  return 0;
+}
 
 // Selected elements (ms[i], ns[i]) of a dense problem, in FP64. For a grouped problem the caller
 // passes the group's A/sA/B/sB base pointers.

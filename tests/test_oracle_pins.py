@@ -11,6 +11,8 @@
   outside the valid region stay untouched.
 * Accumulating form D = C + A·Bᵀ: the hand-worked example with a C added, A = 0 gives C exactly,
   C = 0 gives the plain GEMM bit for bit.
+* K-grouped GEMM: each group equals the dense oracle on its K slice, an empty group gives zeros, one
+  group over all of K equals the dense GEMM bit for bit, and the groups sum to the dense GEMM.
 * Masked GEMM fused with SwiGLU: silu against scipy's logistic function (x·expit(x)) and its limits;
   the fused output against silu(gate)·up formed from the plain masked oracle's two halves.
 * Packed UE8M0 scales: the OCP MX E8M0 table (golden file) and torch's float8_e8m0fnu conversion
@@ -491,3 +493,31 @@ def test_masked_swiglu_equals_silu_gate_times_up():
     assert np.array_equal(H[2], oracle.bf16_from_f64(ref[2]))
     gs, ms, js = np.array([1, 2, 2]), np.array([0, 5, 159]), np.array([0, 255, 128])
     assert np.allclose(oracle.masked_swiglu_sampled(a.A, a.sA, b.B, b.sB, gs, ms, js), ref[gs, ms, js], rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------------------------
+# K-grouped GEMM (groups along K)
+
+
+def test_k_grouped_equals_dense_on_slices():
+    M, N = 40, 136
+    off = np.array([0, 256, 256, 640, 1024], np.int32)        # group 1 is empty
+    K = int(off[-1])
+    a = dg_inputs.make_a(M, K, seed=16)
+    b = dg_inputs.make_b(1, N, K, seed=16)
+    ref = oracle.k_grouped(a.A, a.sA, b.B[0], b.sB[0], off, threads=4)
+    for g in range(len(off) - 1):
+        k0, k1 = int(off[g]), int(off[g + 1])
+        if k0 == k1:
+            assert np.all(ref[g] == 0)
+            continue
+        kb = slice(k0 // 128, k1 // 128)
+        sl, _ = oracle.gemm_nt(np.ascontiguousarray(a.A[:, k0:k1]), np.ascontiguousarray(a.sA[kb]),
+                               np.ascontiguousarray(b.B[0][:, k0:k1]), np.ascontiguousarray(b.sB[0][:, kb]), threads=2)
+        assert np.array_equal(ref[g], sl)
+    full, _ = oracle.gemm_nt(a.A, a.sA, b.B[0], b.sB[0], threads=2)
+    one = oracle.k_grouped(a.A, a.sA, b.B[0], b.sB[0], np.array([0, K], np.int32), threads=2)
+    assert np.array_equal(one[0], full)
+    assert np.allclose(ref.sum(axis=0), full, rtol=1e-12, atol=1e-12 * np.abs(full).max())
+    with pytest.raises(ValueError):
+        oracle.k_grouped(a.A, a.sA, b.B[0], b.sB[0], np.array([0, 100, K], np.int32))
