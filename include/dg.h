@@ -190,6 +190,25 @@ dg_status dg_fp8_gemm_tt_f32(const uint8_t* A, const float* sA, const uint8_t* B
                              int M, int N, int K, dg_stream_t stream);
 
 /*
+ * K-grouped contiguous GEMM (MoE weight backward): grouped along K, with M and N shared by the groups
+ * (k_grouped_fp8_gemm_tn_contiguous, tr.news.hada.io/topic?id=19459, § "Dense ve Grouped GEMM").
+ * The experts' token segments are concatenated along K; segment g is k in [k_offsets[g],
+ * k_offsets[g+1]), and D[g] = Σ over it of A[k,:]ᵀ·B[k,:] with the scales of those K-blocks:
+ *   A  [K_total, M] E4M3 (M contiguous)    sA [K_total/128][align4(M)] FP32 (1x128 K-groups of each m)
+ *   B  [K_total, N] E4M3 (N contiguous)    sB [ceil(N/128)][K_total/128] FP32 (128x128 blocks)
+ *   k_offsets [G+1] int32 on the device: non-decreasing multiples of 128, k_offsets[G] <= K_total
+ *   D  [G, M, N] BF16 bits (or FP32 for _f32). An empty segment gives D[g] = 0.
+ * M and N must be multiples of 16 and K_total of 128. Offsets that break these rules set
+ * DG_DEV_BAD_GROUP_INDEX and leave D[g] of that group untouched. The host never reads k_offsets.
+ */
+dg_status dg_fp8_k_grouped_gemm_tn_contiguous(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                              const int32_t* k_offsets, uint16_t* D, int G, int M, int N,
+                                              int K_total, dg_stream_t stream);
+dg_status dg_fp8_k_grouped_gemm_tn_contiguous_f32(const uint8_t* A, const float* sA, const uint8_t* B,
+                                                  const float* sB, const int32_t* k_offsets, float* D, int G, int M,
+                                                  int N, int K_total, dg_stream_t stream);
+
+/*
  * Masked grouped GEMM fused with SwiGLU (MoE decode): the up/gate projection of each expert and the
  * SwiGLU after it in one kernel, so the 2I-wide intermediate never reaches memory. It is the first
  * fusion of the pages' Mega MoE, which fuses linear 1, SwiGLU and linear 2 of the experts

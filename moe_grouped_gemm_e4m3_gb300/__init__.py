@@ -12,6 +12,8 @@ The names mirror the C ABI:
 * ``*_f32`` variants store the FP32 accumulator instead of BF16 (same kernel and order).
 * ``dg_fp8_gemm_{nn,tn,tt}(A, sA, B, sB, D, M=, N=, K=)``     dense D = A·Bᵀ with A stored [K,M] (t) and/or
   B stored [K,N] (second letter n); the scales keep dg_fp8_gemm_nt's layouts
+* ``dg_fp8_k_grouped_gemm_tn_contiguous(A, sA, B, sB, k_offsets, D)``  groups along K: A [K,M], B [K,N],
+  D [G,M,N]
 * ``dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H)``  masked GEMM + SwiGLU: B [G, 2I, K], H [G, M_max, I]
 * ``dg_fp8_gemm_nt_acc_f32(A, sA, B, sB, C, D)``             D = C + A·Bᵀ (FP32 C and D; C may be D)
 * ``*_ue8m0`` variants take power-of-two scales as packed UE8M0 int32 words (four K-groups per
@@ -39,7 +41,8 @@ __all__ = [
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
-    "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
+    "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
+    "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
     "DG_DEV_TIMEOUT",
 ]
@@ -58,6 +61,7 @@ EXPORTED_SYMBOLS = (
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
+    "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32",
 )
 
 
@@ -106,6 +110,9 @@ def load(build_if_missing: bool = True):
     for name in ("dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, P]
+    for name in ("dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
     for name in ("dg_query_config", "dg_query_config_ue8m0"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
@@ -279,6 +286,28 @@ def dg_fp8_gemm_tt(A, sA, B, sB, D, M, N, K, stream=None):
 
 def dg_fp8_gemm_tt_f32(A, sA, B, sB, D, M, N, K, stream=None):
     return _dense_layout("dg_fp8_gemm_tt_f32", True, A, sA, B, sB, D, M, N, K, stream)
+
+
+def _k_grouped(name, f32, A, sA, B, sB, k_offsets, D, stream):
+    import torch
+    lib = load()
+    K_total, M = A.shape
+    N = B.shape[1]
+    G = k_offsets.shape[0] - 1
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", _f32()), _ptr(k_offsets, "k_offsets", (torch.int32,)),
+                              _ptr(D, "D", _d_types(f32)), G, M, N, K_total, _stream(stream)))
+    return D
+
+
+def dg_fp8_k_grouped_gemm_tn_contiguous(A, sA, B, sB, k_offsets, D, stream=None):
+    """Groups along K: A [K_total, M], B [K_total, N], k_offsets [G+1] int32 (multiples of 128),
+    D [G, M, N] (bfloat16) = Σ over each group's K range."""
+    return _k_grouped("dg_fp8_k_grouped_gemm_tn_contiguous", False, A, sA, B, sB, k_offsets, D, stream)
+
+
+def dg_fp8_k_grouped_gemm_tn_contiguous_f32(A, sA, B, sB, k_offsets, D, stream=None):
+    return _k_grouped("dg_fp8_k_grouped_gemm_tn_contiguous_f32", True, A, sA, B, sB, k_offsets, D, stream)
 
 
 def dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H, stream=None):

@@ -417,6 +417,86 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   return DG_OK;
 }
 
+// The K-grouped GEMM: A stored [K_total, M], B stored [K_total, N] (both MN-major), D [G, M, N];
+// group g sums the K-blocks [offsets[g], offsets[g+1]) / 128 (offsets on the device).
+dg_status run_k_grouped(bool out_f32, const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                        const int32_t* offsets, void* D, int G, int M, int N, int K_total, cudaStream_t stream) {
+  t_last_error.clear();
+  if (G < 0 || M < 0 || N < 0 || K_total < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
+  if (G == 0 || M == 0 || N == 0) return DG_OK;
+  if (!A || !sA || !B || !sB || !offsets || !D) return fail(DG_ERR_INVALID_ARG, "null pointer");
+  if (M % 16 != 0 || N % 16 != 0)
+    return fail(DG_ERR_ALIGNMENT, "K-grouped: M and N must be multiples of 16 (A [K,M], B [K,N] rows)");
+  if (K_total % 128 != 0) return fail(DG_ERR_ALIGNMENT, "K-grouped: K_total must be a multiple of 128");
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16))
+    return fail(DG_ERR_ALIGNMENT, "A, B and D must be 16-byte aligned");
+  if (!aligned(sA, 4) || !aligned(sB, 4) || !aligned(offsets, 4))
+    return fail(DG_ERR_ALIGNMENT, "sA, sB and offsets must be 4-byte aligned");
+  if ((long long)G * M > INT_MAX - 256 || K_total > INT_MAX - 256 || N > INT_MAX - 256)
+    return fail(DG_ERR_UNSUPPORTED, "a tensor extent exceeds 2^31 - 257");
+  if (K_total == 0) {   // every group is empty: D = 0
+    const cudaError_t e = cudaMemsetAsync(D, 0, (size_t)G * M * N * (out_f32 ? 4 : 2), stream);
+    return e == cudaSuccess ? DG_OK : fail_cuda(e, "cudaMemsetAsync(D)");
+  }
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  const int sms = effective_sms(*st);
+  const int bn = N > 128 ? 256 : 128;
+  const int mb = ceil_div(M, 128), nb = ceil_div(N, bn);
+  if ((long long)G * mb * nb > INT_MAX / 2) return fail(DG_ERR_UNSUPPORTED, "too many tiles");
+  const int tiles = G * mb * nb;
+
+  dg::LaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  dg::GemmParams& p = a.p;
+  p.M = M;
+  p.N = N;
+  p.K = K_total;
+  p.G = G;
+  p.nkb = K_total / 128;
+  p.nnb = ceil_div(N, 128);
+  p.ldsa = dg_get_tma_aligned_size(M, 4);
+  p.num_m_blocks = mb;
+  p.num_n_blocks = nb;
+  p.num_splits = 1;
+  p.kb_per_split = p.nkb;
+  p.num_tiles = tiles;
+  p.raster_m = mb < 16 ? mb : 16;
+  p.sA = sA;
+  p.sB = sB;
+  p.D = D;
+  p.status = st->status;
+  p.a_mn = 1;
+  p.b_mn = 1;
+  p.k_offsets = offsets;
+  p.k_total = K_total;
+  if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)M, (uint64_t)K_total, (uint64_t)M, 128, 128,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
+    return s;
+  if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)N, (uint64_t)K_total, (uint64_t)N, 128, 128,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
+    return s;
+  const uint64_t d_rows = (uint64_t)G * M;
+  if (out_f32)
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)N, d_rows, (uint64_t)N * 4, 16, 32,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
+  else
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, d_rows, (uint64_t)N * 2, 32, 32,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
+  if (s != DG_OK) return s;
+  a.block_n = bn;
+  a.out_f32 = out_f32;
+  a.grid = tiles < sms ? tiles : sms;
+  a.stream = stream;
+  if (print_configs())
+    std::fprintf(stderr, "[dg] k-grouped%s G=%d M=%d N=%d K_total=%d: BM=128 BN=%d grid=%d tiles=%d\n",
+                 out_f32 ? "/f32" : "", G, M, N, K_total, bn, a.grid, tiles);
+  const cudaError_t e = dg::launch_kgrouped(a);
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return DG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -493,6 +573,18 @@ dg_status dg_fp8_grouped_masked_ue8m0_f32(const uint8_t* A, const int32_t* sA, c
                                           dg_stream_t stream) {
   return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, D, M_max, N, K, G, static_cast<cudaStream_t>(stream),
                   true);
+}
+
+dg_status dg_fp8_k_grouped_gemm_tn_contiguous(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                              const int32_t* k_offsets, uint16_t* D, int G, int M, int N,
+                                              int K_total, dg_stream_t stream) {
+  return run_k_grouped(false, A, sA, B, sB, k_offsets, D, G, M, N, K_total, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_k_grouped_gemm_tn_contiguous_f32(const uint8_t* A, const float* sA, const uint8_t* B,
+                                                  const float* sB, const int32_t* k_offsets, float* D, int G, int M,
+                                                  int N, int K_total, dg_stream_t stream) {
+  return run_k_grouped(true, A, sA, B, sB, k_offsets, D, G, M, N, K_total, static_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_fp8_gemm_nn(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int M,

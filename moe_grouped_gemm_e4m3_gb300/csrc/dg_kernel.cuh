@@ -44,7 +44,9 @@
 
 namespace dg {
 
-enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+// kKGrouped: groups along K (A stored [K_total, M], B stored [K_total, N], D [G, M, N]); every group
+// covers all M x N tiles over its own K-block range.
+enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kKGrouped = 3 };
 
 constexpr int kStatusBadGroup = 0x1;
 constexpr int kStatusBadMaskedM = 0x2;
@@ -69,6 +71,8 @@ struct GemmParams {
   int accumulate;       // FP32 D only: add the result to D (D = C + A·Bᵀ with D holding C)
   int swiglu_i;         // fused SwiGLU: I, the width of H; B holds 2I rows per group (gate, then up)
   int a_mn, b_mn;       // dense layouts: A stored [K,M] / B stored [K,N] (MN-major) instead of K-major
+  const int32_t* k_offsets;  // K-grouped: [G+1] K offsets of the groups (multiples of 128), on the device
+  int k_total;          // K-grouped: extent of A and B along K
   const int32_t* m_indices;
   const int32_t* masked_m;
   void* D;           // row-major, row stride N elements (used by predicated stores)
@@ -164,16 +168,23 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, int lane
     // u -> (m_blk, n_blk) rasterised in groups of raster_m m-blocks: the CTAs running at the same
     // time cover raster_m m-blocks x (grid / raster_m) n-blocks, so A and B tiles are re-read
     // from L2 rather than HBM.
+    int v = u;   // tile within its group (K-grouped) or within the problem
+    if constexpr (MODE == kKGrouped) {
+      // one K group per block of num_m_blocks x num_n_blocks tiles
+      const int tiles_per_group = p.num_m_blocks * p.num_n_blocks;
+      tile.g = u / tiles_per_group;
+      v = u - tile.g * tiles_per_group;
+    }
     const int per_group = p.raster_m * p.num_n_blocks;
-    const int grp = u / per_group;
+    const int grp = v / per_group;
     const int first_m = grp * p.raster_m;
     const int gsz = min(p.num_m_blocks - first_m, p.raster_m);
-    const int local = u % per_group;
+    const int local = v % per_group;
     tile.m_blk = first_m + local % gsz;
     tile.n_blk = local / gsz;
     tile.a_row = tile.m_blk * 128;
     tile.rows = min(128, p.M - tile.a_row);
-    tile.g = 0;
+    if constexpr (MODE != kKGrouped) tile.g = 0;
     if constexpr (MODE == kContiguous) {
       // The block's group is the largest valid index among its rows (padding rows are -1).
       // Rows with an index outside [-1, G) are flagged and never stored.
@@ -192,6 +203,18 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, int lane
       tile.g = g;
       if (g < 0) tile.skip = true;               // all padding (or all invalid): nothing to do
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kStatusBadGroup);
+    }
+    if constexpr (MODE == kKGrouped) {
+      // the group's K-block range; an empty range still stores its (zero) tile. Offsets that are
+      // not multiples of 128, decrease or pass k_total are flagged and the group is left untouched.
+      const int k0 = __ldg(p.k_offsets + tile.g), k1 = __ldg(p.k_offsets + tile.g + 1);
+      if ((k0 | k1) % 128 != 0 || k0 < 0 || k1 < k0 || k1 > p.k_total) {
+        tile.skip = true;
+        if (lane == 0 && tile.m_blk == 0 && tile.n_blk == 0) atomicOr(p.status, kStatusBadGroup);
+      }
+      tile.kb0 = k0 / 128;
+      tile.kb1 = k1 / 128;
+      tile.a_row = tile.g * p.M + tile.m_blk * 128;   // the tile's first row of D [G*M, N]
     }
   }
   return tile;
@@ -368,7 +391,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
         const Tile tile = decode_tile<BN, MODE>(p, t, lane);
         if (tile.skip) continue;
-        const int b_row = tile.g * p.N + tile.n_blk * BN;
+        const int b_row = (MODE == kKGrouped ? 0 : tile.g * p.N) + tile.n_blk * BN;
         // Lane 0 runs the tile's K loop on its own (no warp-wide step per K-block).
         int ok = 1;
         if (lane == 0) {
@@ -380,7 +403,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             uint8_t* sa = smem + s * Plan::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
             if (p.a_mn)   // A stored [K, M]: the box is 128 K-rows x 128 M-bytes
-              tma_load_2d(&tmA, sa, &full_bar[s], tile.a_row, kb * 128, policy);
+              tma_load_2d(&tmA, sa, &full_bar[s], MODE == kKGrouped ? tile.m_blk * 128 : tile.a_row, kb * 128,
+                          policy);
             else
               tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
             if (p.b_mn) {  // B stored [K, N]: BN/128 boxes of 128 K-rows x 128 N-bytes, 16 KB apart
@@ -507,7 +531,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       // first column of this warp (as a row of B: fused SwiGLU puts the up rows at I + 128·n)
       const int n_col0 = SWIGLU ? (cgrp ? p.swiglu_i : 0) + tile.n_blk * 128 : tile.n_blk * BN + cgrp * EPI_COLS;
       const bool col_exists = n_col0 < p.N;
-      const float* sb_ptr = p.sB + ((size_t)tile.g * p.nnb + (col_exists ? n_col0 / 128 : 0)) * p.nkb;
+      const float* sb_ptr = p.sB + ((size_t)(MODE == kKGrouped ? 0 : tile.g) * p.nnb + (col_exists ? n_col0 / 128 : 0)) * p.nkb;
       // Warps with no row or no column in range only keep the TMEM handshake going.
       const bool active = col_exists && __any_sync(0xffffffffu, row_exists);
 
@@ -515,8 +539,10 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       for (int i = 0; i < EPI_COLS; ++i) acc[i] = 0.0f;
 
       // scales of the first K-block; later ones are fetched one K-block ahead
-      float sa_next = (active && row_exists) ? __ldg(sa_ptr + (size_t)kb_begin * p.ldsa) : 0.0f;
-      float sb_next = active ? __ldg(sb_ptr + kb_begin) : 0.0f;
+      // (a K-grouped tile can have an empty K range: it stores zeros and reads no scale)
+      const bool any_kb = kb_begin < kb_end;
+      float sa_next = (active && row_exists && any_kb) ? __ldg(sa_ptr + (size_t)kb_begin * p.ldsa) : 0.0f;
+      float sb_next = (active && any_kb) ? __ldg(sb_ptr + kb_begin) : 0.0f;
 
       for (int kb = kb_begin; kb < kb_end; ++kb, ++acc_it) {
         const int b = acc_it % NBUF;
@@ -722,7 +748,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
 
       // ---------------- output
       bool write_row;
-      if constexpr (MODE == kDense) {
+      if constexpr (MODE == kDense || MODE == kKGrouped) {
         write_row = row_exists;
       } else if constexpr (MODE == kMasked) {
         write_row = row_exists;   // rows counts only the valid rows of the group

@@ -32,6 +32,8 @@ constexpr int tmem_bufs_for(int block_n) { return 512 / block_n; }
 cudaError_t launch_dense(const LaunchArgs& a);
 cudaError_t launch_contiguous(const LaunchArgs& a);
 cudaError_t launch_masked(const LaunchArgs& a);
+// The K-grouped form (groups along K; FP32-scale kernel, MN-major A and B).
+cudaError_t launch_kgrouped(const LaunchArgs& a);
 // The masked form fused with SwiGLU (block_n 256, FP32-scale kernel).
 cudaError_t launch_masked_swiglu(const LaunchArgs& a);
 // The block-scaled kernel for packed UE8M0 scales (block_n is always 256).
