@@ -332,25 +332,18 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.num_m_blocks = ceil_div(rows, 128);
   p.num_n_blocks = swiglu ? d_cols / 128 : ceil_div(N, cfg.block_n);
   p.swiglu_i = swiglu ? d_cols : 0;
-  p.a_mn = a_mn ? 1 : 0;
-  p.b_mn = b_mn ? 1 : 0;
+  p.flags = (a_mn ? dg::kFlagAMN : 0) | (b_mn ? dg::kFlagBMN : 0) | (accumulate ? dg::kFlagAccumulate : 0);
   p.num_splits = cfg.splits;
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles * cfg.splits;
   p.raster_m = cfg.raster_m;
-  p.nkq = ceil_div(p.nkb, 4);
-  if (block_scaled) {
-    p.sfa = static_cast<const uint32_t*>(sA);
-    p.sfb = static_cast<const uint32_t*>(sB);
-  } else {
-    p.sA = static_cast<const float*>(sA);
-    p.sB = static_cast<const float*>(sB);
-  }
+  // (the block-scaled kernel reads these as its packed UE8M0 words)
+  p.sA = static_cast<const float*>(sA);
+  p.sB = static_cast<const float*>(sB);
   p.m_indices = mode == dg::kContiguous ? idx : nullptr;
   p.masked_m = mode == dg::kMasked ? idx : nullptr;
   p.D = D;
   p.status = st->status;
-  p.accumulate = accumulate ? 1 : 0;
   if (accumulate && static_cast<const void*>(C) != D) {
     cudaError_t ce = cudaMemcpyAsync(D, C, (size_t)rows * N * sizeof(float), cudaMemcpyDeviceToDevice, stream);
     if (ce != cudaSuccess) return fail_cuda(ce, "cudaMemcpyAsync(C -> D)");
@@ -467,10 +460,8 @@ dg_status run_k_grouped(bool out_f32, const uint8_t* A, const float* sA, const u
   p.sB = sB;
   p.D = D;
   p.status = st->status;
-  p.a_mn = 1;
-  p.b_mn = 1;
-  p.k_offsets = offsets;
-  p.k_total = K_total;
+  p.flags = dg::kFlagAMN | dg::kFlagBMN;
+  p.m_indices = offsets;   // the K offsets of the groups
   if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)M, (uint64_t)K_total, (uint64_t)M, 128, 128,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
     return s;

@@ -51,6 +51,7 @@ enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kKGrouped = 3 };
 constexpr int kStatusBadGroup = 0x1;
 constexpr int kStatusBadMaskedM = 0x2;
 
+// Kept at 128 bytes: a larger parameter block made ptxas spill the contiguous form's epilogue.
 struct GemmParams {
   int M;             // dense: M; contiguous: M_total; masked: M_max (rows per group)
   int N, K, G;
@@ -63,23 +64,23 @@ struct GemmParams {
   int kb_per_split;  // K-blocks per split (the last split may get fewer)
   int num_tiles;     // dense/contiguous: m_blocks * n_blocks * splits; masked: computed on device
   int raster_m;      // m-blocks per rasterisation group
-  const float* sA;
-  const float* sB;
-  const uint32_t* sfa;  // packed UE8M0 scales (block-scaled kernel): [G][ceil(nkb/4)][ldsa]
-  const uint32_t* sfb;  // packed UE8M0 scales (block-scaled kernel): [G][nnb][ceil(nkb/4)]
-  int nkq;              // ceil(nkb / 4): packed scale words along K
-  int accumulate;       // FP32 D only: add the result to D (D = C + A·Bᵀ with D holding C)
-  int swiglu_i;         // fused SwiGLU: I, the width of H; B holds 2I rows per group (gate, then up)
-  int a_mn, b_mn;       // dense layouts: A stored [K,M] / B stored [K,N] (MN-major) instead of K-major
-  const int32_t* k_offsets;  // K-grouped: [G+1] K offsets of the groups (multiples of 128), on the device
-  int k_total;          // K-grouped: extent of A and B along K
-  const int32_t* m_indices;
+  const float* sA;           // block-scaled kernel: the packed UE8M0 words (uint32) instead
+  const float* sB;           // block-scaled kernel: the packed UE8M0 words (uint32) instead
+  const int32_t* m_indices;  // K-grouped: the [G+1] K offsets of the groups (K is then K_total)
   const int32_t* masked_m;
   void* D;           // row-major, row stride N elements (used by predicated stores)
   float* workspace;  // split-K partial tiles
   int* counters;     // split-K arrival counter per output tile (zero between calls)
   int* status;       // device status word
+  int flags;         // kFlag* bits below
+  int swiglu_i;      // fused SwiGLU: I, the width of H; B holds 2I rows per group (gate, then up)
 };
+
+static_assert(sizeof(GemmParams) <= 128, "keep the kernel parameter block at 128 bytes (register allocation)");
+
+constexpr int kFlagAccumulate = 0x1;  // FP32 D only: add the product onto D (D = C + A·Bᵀ, D holding C)
+constexpr int kFlagAMN = 0x2;         // dense layouts: A stored [K, M] (MN-major)
+constexpr int kFlagBMN = 0x4;         // dense layouts: B stored [K, N] (MN-major)
 
 struct Tile {
   int g;          // group
@@ -207,8 +208,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, int lane
     if constexpr (MODE == kKGrouped) {
       // the group's K-block range; an empty range still stores its (zero) tile. Offsets that are
       // not multiples of 128, decrease or pass k_total are flagged and the group is left untouched.
-      const int k0 = __ldg(p.k_offsets + tile.g), k1 = __ldg(p.k_offsets + tile.g + 1);
-      if ((k0 | k1) % 128 != 0 || k0 < 0 || k1 < k0 || k1 > p.k_total) {
+      const int k0 = __ldg(p.m_indices + tile.g), k1 = __ldg(p.m_indices + tile.g + 1);
+      if ((k0 | k1) % 128 != 0 || k0 < 0 || k1 < k0 || k1 > p.K) {
         tile.skip = true;
         if (lane == 0 && tile.m_blk == 0 && tile.n_blk == 0) atomicOr(p.status, kStatusBadGroup);
       }
@@ -402,12 +403,12 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             if (!ok) break;
             uint8_t* sa = smem + s * Plan::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
-            if (p.a_mn)   // A stored [K, M]: the box is 128 K-rows x 128 M-bytes
+            if (p.flags & kFlagAMN)   // A stored [K, M]: the box is 128 K-rows x 128 M-bytes
               tma_load_2d(&tmA, sa, &full_bar[s], MODE == kKGrouped ? tile.m_blk * 128 : tile.a_row, kb * 128,
                           policy);
             else
               tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
-            if (p.b_mn) {  // B stored [K, N]: BN/128 boxes of 128 K-rows x 128 N-bytes, 16 KB apart
+            if (p.flags & kFlagBMN) {  // B stored [K, N]: BN/128 boxes of 128 K-rows x 128 N-bytes, 16 KB apart
 #pragma unroll
               for (int h = 0; h < BN / 128; ++h)
                 tma_load_2d(&tmB, sa + Plan::kABytes + h * 128 * 128, &full_bar[s], b_row + h * 128, kb * 128,
@@ -459,13 +460,14 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
-            const uint64_t adesc = p.a_mn ? make_sw128_mnmajor_desc(a_addr, 128 * 128) : make_sw128_kmajor_desc(a_addr);
-            const uint64_t bdesc = p.b_mn ? make_sw128_mnmajor_desc(a_addr + Plan::kABytes, 128 * 128)
-                                          : make_sw128_kmajor_desc(a_addr + Plan::kABytes);
+            const bool a_mn = (p.flags & kFlagAMN) != 0, b_mn = (p.flags & kFlagBMN) != 0;
+            const uint64_t adesc = a_mn ? make_sw128_mnmajor_desc(a_addr, 128 * 128) : make_sw128_kmajor_desc(a_addr);
+            const uint64_t bdesc = b_mn ? make_sw128_mnmajor_desc(a_addr + Plan::kABytes, 128 * 128)
+                                        : make_sw128_kmajor_desc(a_addr + Plan::kABytes);
             // one K=32 step: +32 bytes inside a K-major 128-byte row (+2 in the >>4 address field), or
             // +32 rows of 128 bytes in an MN-major tile (+256)
-            const uint32_t a_step = p.a_mn ? 256u : 2u, b_step = p.b_mn ? 256u : 2u;
-            const uint32_t idesc = kIdesc | ((uint32_t)p.a_mn << 15) | ((uint32_t)p.b_mn << 16);
+            const uint32_t a_step = a_mn ? 256u : 2u, b_step = b_mn ? 256u : 2u;
+            const uint32_t idesc = kIdesc | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
             const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -795,7 +797,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (OUT_F32 && p.accumulate)
+            if (OUT_F32 && (p.flags & kFlagAccumulate))
               tma_reduce_add_2d(&tmD, staging + sel * Plan::kStagingBox, n_col0 + chunk * kColsPerBox,
                                 tile.a_row + quad * 32);
             else
@@ -814,7 +816,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           for (int j = 0; j < EPI_COLS; j += 4) {
             if (n_col0 + j < p.N) {
               float* dst = drow + n_col0 + j;
-              if (p.accumulate) {
+              if (p.flags & kFlagAccumulate) {
                 atomicAdd(dst, acc[j]); atomicAdd(dst + 1, acc[j + 1]);
                 atomicAdd(dst + 2, acc[j + 2]); atomicAdd(dst + 3, acc[j + 3]);
               } else {

@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       // Warp 8 also posts each tile's description (then an end mark) for the epilogue, which
       // thereby never decodes tiles itself.
       const int q = warp % 4;                  // TMEM lane quadrant of this warp
+      const int nkq = (p.nkb + 3) / 4;         // packed scale words along K
       const uint32_t lane_base = (uint32_t)(q * 32) << 16;
       const bool poster = (warp == R::kScaleWarp0);
       uint32_t sf_it = 0, desc_it = 0;
@@ -289,15 +290,15 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         const int row_in_tile = q * 32 + lane;
         const bool row_exists = row_in_tile < tile.rows;
         const int m_local = tile.m_blk * 128 + row_in_tile;
-        const uint32_t* sfa_ptr = p.sfa + (MODE == kMasked ? (size_t)tile.g * p.nkq * p.ldsa : 0) + m_local;
+        const uint32_t* sfa_ptr = reinterpret_cast<const uint32_t*>(p.sA) + (MODE == kMasked ? (size_t)tile.g * nkq * p.ldsa : 0) + m_local;
         const int nb0 = tile.n_blk * 2;        // the tile's two 128-row scale blocks of B
-        const uint32_t* sfb_ptr = p.sfb + ((size_t)tile.g * p.nnb + nb0) * p.nkq;
+        const uint32_t* sfb_ptr = reinterpret_cast<const uint32_t*>(p.sB) + ((size_t)tile.g * p.nnb + nb0) * nkq;
         const bool has_nb1 = nb0 + 1 < p.nnb;
         const int q_end = (tile.kb1 - 1) >> 2;
         for (int quad = tile.kb0 >> 2; quad <= q_end; ++quad, ++sf_it) {
           const uint32_t a = row_exists ? __ldg(sfa_ptr + (size_t)quad * p.ldsa) : 0x7F7F7F7Fu;
           const uint32_t b0 = __ldg(sfb_ptr + quad);
-          const uint32_t b1 = has_nb1 ? __ldg(sfb_ptr + p.nkq + quad) : 0x7F7F7F7Fu;
+          const uint32_t b1 = has_nb1 ? __ldg(sfb_ptr + nkq + quad) : 0x7F7F7F7Fu;
           const uint32_t slot = sf_it % SLOTS;
           if (!mbar_wait(&sf_empty_bar[slot], ((sf_it / SLOTS) & 1) ^ 1, abort_flag, p.status)) {
             alive = false;
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (OUT_F32 && p.accumulate)
+            if (OUT_F32 && (p.flags & kFlagAccumulate))
               tma_reduce_add_2d(&tmD, staging + sel * Plan::kStagingBox, n_col0 + chunk * kColsPerBox,
                                 tile.a_row + quad * 32);
             else
@@ -498,7 +499,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
           for (int j = 0; j < EPI_COLS; j += 4) {
             if (n_col0 + j < p.N) {
               float* dst = drow + n_col0 + j;
-              if (p.accumulate) {
+              if (p.flags & kFlagAccumulate) {
                 atomicAdd(dst, acc[j]); atomicAdd(dst + 1, acc[j + 1]);
                 atomicAdd(dst + 2, acc[j + 2]); atomicAdd(dst + 3, acc[j + 3]);
               } else {
