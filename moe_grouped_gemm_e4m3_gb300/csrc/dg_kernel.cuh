@@ -282,8 +282,11 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
 
-// silu(x) = x / (1 + e^-x), the gate function of SwiGLU.
-__device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
+// silu(x) = x / (1 + e^-x), the gate function of SwiGLU, with the fast exponential and division
+// (relative error ~1e-6). For x below about -87 the denominator overflows and the quotient is -0, the
+// function's limit. (An IEEE-rounded division or reciprocal there takes a slow special-case path:
+// it made the fused kernel 50% slower than the GEMM alone on decode-sized outputs.)
+__device__ __forceinline__ float silu_f32(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {
