@@ -4,8 +4,10 @@
 Workload (one "step"): the dense FP8 GEMM sweep — M in {64, 128, 4096} x (N, K) in {(2112, 7168),
 (24576, 1536), (32768, 512), (7168, 16384), (4096, 7168), (7168, 2048)}, A[M,K] and B[N,K] drawn
 N(0,1) from seed 0 and quantised to E4M3 (1x128 A scales, 128x128 B scales, amax/448), BF16 D.
-Each of the 18 GEMMs is one launch of the sm_103a kernel through the C ABI; an L2 flush (a write
-of a 256 MB buffer) precedes every GEMM and lies outside the CUDA events that time it.
+Each of the 18 GEMMs is one launch of the sm_103a kernel through the C ABI; an L2 flush precedes
+every GEMM and lies outside the CUDA events that time it: a write of a 256 MB buffer, then a read of
+a second 256 MB buffer, so that the write's dirty lines have reached HBM (and L2 holds only clean,
+unrelated lines) when the GEMM starts.
 
 Metric: useful TFLOP/s = sum(2*M*N*K) / sum(GEMM time). Printed as one JSON line with the
 roofline of the dominant kernel, the CPU oracle baseline, the end-to-end number through host
@@ -46,8 +48,25 @@ SHAPES = [(M, N, K) for M in SWEEP_M for (N, K) in SWEEP_NK]
 WORKLOAD = "dense FP8 E4M3 GEMM sweep, M in {64,128,4096} x (N,K) in {(2112,7168),(24576,1536),(32768,512),(7168,16384),(4096,7168),(7168,2048)}"
 METRIC = "FP8 TFLOPS (2MNK/s) per shape; % of GB300 FP8 dense peak or HBM GB/s"
 L2_FLUSH_BYTES = 256 << 20
+L2_NOTE = ("flushed before every GEMM, outside its CUDA events: a 256 MB write, then a 256 MB read of a "
+           "second buffer (the write's dirty lines reach HBM before the GEMM starts)")
 CPU_SAMPLE_PER_SHAPE = 196608
 UE8M0 = False      # set by --scales ue8m0
+
+
+class L2Flush:
+    """Evicts the GEMM's operands from L2: writes a buffer larger than L2, then reads another one, so
+    that the eviction's write-back of dirty lines happens here and not inside the timed GEMM."""
+
+    def __init__(self):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.zeros(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def __call__(self, i):
+        import torch
+        self.w.fill_(i & 0xFF)
+        self.sink = self.r.view(torch.float32).sum()   # one reduction kernel reading 256 MB (zeros)
 
 
 def parse_args():
@@ -269,12 +288,12 @@ def run_ours(args, rank, world, local):
         tensors.append(dict(M=M, N=N, K=K, A=dev(a.A), sA=dev(gsA), B=dev(b.B[0]), sB=dev(gsB[0]),
                             D=torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
                             cfg=query_config(dg, 0, M, N, K)))
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
 
     def one_step(events):
         for i, t in enumerate(tensors):
-            flush.fill_(i & 0xFF)
+            flush(i)
             if events is not None:
                 events[i][0].record(stream)
             gemm(t["A"], t["sA"], t["B"], t["sB"], t["D"], stream)
@@ -397,7 +416,9 @@ def run_ours(args, rank, world, local):
                   "e4m3 x e4m3 -> f32 accumulate (fine-grained scales) -> bf16"),
         "config": {"workload": WORKLOAD if len(tensors) == 18 else f"subset {SHAPES}", "shapes": len(tensors), "seed": 0, "values": "N(0,1)",
                    "quantisation": quantisation_note(),
-                   "l2": "256 MB write before every GEMM, outside the GEMM's CUDA events",
+                   "l2": L2_NOTE,
+                   "e2e": ("every step: H2D of each GEMM's A, sA, B, sB from pinned host memory, the GEMM, D2H "
+                           "of D to pinned host memory; copies on two copy streams, overlapping the GEMMs"),
                    "parallelism": f"replicas x{world}", "wall_ms_per_step": round((t1 - t0) * 1e3 / args.steps, 4)},
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -412,8 +433,10 @@ def run_ours(args, rank, world, local):
 
 
 def measure_e2e(dg, problems, args, stream):
-    """Same sweep through host buffers: H2D of A, sA, B, sB from pinned memory, the GEMM, and the
-    D2H of D, all inside the timed region."""
+    """Same sweep through host buffers: every step copies each GEMM's A, sA, B, sB from pinned host
+    memory, runs the GEMM and copies D back to pinned host memory, all inside the timed region.
+    The copies are pipelined across three streams (host-to-device, compute, device-to-host), so the
+    two copy directions overlap each other and the GEMMs; a step ends when its last D is on the host."""
     import torch
     host = []
     h2d = d2h = 0
@@ -430,30 +453,41 @@ def measure_e2e(dg, problems, args, stream):
         h["D"] = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
         d2h += M * N * 2
         host.append(h)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    done = [torch.cuda.Event() for _ in host]       # the GEMM of shape i has finished (inputs read, D written)
+    out_done = [torch.cuda.Event() for _ in host]   # D of shape i is on the host
     steps = max(3, min(args.steps, 10))
 
-    def one_step(evs):
+    def one_step():
+        ev_in = []
         for i, h in enumerate(host):
-            flush.fill_(i & 0xFF)
-            if evs is not None:
-                evs[i][0].record(stream)
-            for name in ("A", "sA", "B", "sB"):
-                h["d" + name].copy_(h[name], non_blocking=True)
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(done[i])             # the previous step's GEMM i no longer reads them
+                for name in ("A", "sA", "B", "sB"):
+                    h["d" + name].copy_(h[name], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s_in)
+                ev_in.append(e)
+        for i, h in enumerate(host):
+            stream.wait_event(ev_in[i])
+            stream.wait_event(out_done[i])            # the previous step's D2H no longer reads D
             gemm(h["dA"], h["dsA"], h["dB"], h["dsB"], h["dD"], stream)
-            h["D"].copy_(h["dD"], non_blocking=True)
-            if evs is not None:
-                evs[i][1].record(stream)
+            done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done[i])
+                h["D"].copy_(h["dD"], non_blocking=True)
+                out_done[i].record(s_out)
 
-    one_step(None)
-    one_step(None)
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in host]
-          for _ in range(steps)]
+    one_step()
+    one_step()
     torch.cuda.synchronize()
-    for s in range(steps):
-        one_step(ev[s])
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(s_in)
+    for _ in range(steps):
+        one_step()
+    t_end.record(s_out)
     torch.cuda.synchronize()
-    ms = float(np.mean([sum(e[0].elapsed_time(e[1]) for e in ev[s]) for s in range(steps)]))
+    ms = t_start.elapsed_time(t_end) / steps
     flops = sum(2.0 * h["M"] * h["N"] * h["K"] for h in host)
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
@@ -561,14 +595,14 @@ def run_all_configs(args):
     peaks = load_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     reps = max(3, min(args.steps, 20))
 
     def timeit(fn):
         fn()
         ts = []
         for r in range(reps):
-            flush.fill_(r & 0xFF)
+            flush(r)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
