@@ -281,6 +281,21 @@ int dg_get_mk_alignment_for_contiguous_layout(void);
 void dg_set_num_sms(int n);
 int dg_get_num_sms(void);
 
+/* Tail split of the FP32-scale kernels (dense, contiguous and masked forms, not the fused SwiGLU;
+   calls whose configuration already splits K are unaffected). When the output tiles of a launch
+   leave a last, partial wave of at most half the grid, the kernel may cut each of those tiles into
+   up to n K ranges, computed by otherwise idle SMs and summed in range order (deterministic) by the
+   last range to finish, exactly as split-K does. The kernel takes the split only when its cost model
+   says the K-blocks saved outweigh the exchange. n = 1 switches the tail split off; n <= 0 restores
+   the default (4); values above 16 are clamped. The environment variable DG_TAIL_SPLITS sets the
+   initial value. Returns the previous value. This is a scheduling choice: results stay within the
+   accuracy bar either way, but the tail tiles' FP32 rounding differs between the two settings.
+   Source: it extends the unified (persistent) block scheduler of the feature list on
+   biggo.id/news/202502260712_DeepGEMM_FFMA_Optimization, § "Fitur Utama dan Persyaratan DeepGEMM".
+   The pages do not describe splitting K; the tail rule is this implementation's choice for GB300's
+   152 SMs. */
+int dg_set_tail_splits(int n);
+
 /* Reads and clears the device status word of the current device after synchronising `stream`.
    *code receives the DG_DEV_* bits. Returns DG_ERR_DEVICE_STATUS when a bit was set. */
 dg_status dg_get_device_status(int* code, dg_stream_t stream);

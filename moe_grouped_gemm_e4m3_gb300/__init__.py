@@ -55,7 +55,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32",
     "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_get_tma_aligned_size",
     "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms", "dg_get_num_sms", "dg_get_device_status",
-    "dg_last_error_string", "dg_query_config", "dg_fp8_gemm_nt_noalloc",
+    "dg_last_error_string", "dg_query_config", "dg_fp8_gemm_nt_noalloc", "dg_set_tail_splits",
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
@@ -105,6 +105,7 @@ def load(build_if_missing: bool = True):
     lib.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
     lib.dg_set_num_sms.restype, lib.dg_set_num_sms.argtypes = None, [i32]
     lib.dg_get_num_sms.restype, lib.dg_get_num_sms.argtypes = i32, []
+    lib.dg_set_tail_splits.restype, lib.dg_set_tail_splits.argtypes = i32, [i32]
     lib.dg_get_device_status.restype, lib.dg_get_device_status.argtypes = i32, [ctypes.POINTER(i32), P]
     lib.dg_last_error_string.restype, lib.dg_last_error_string.argtypes = ctypes.c_char_p, []
     for name in ("dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32"):
@@ -359,6 +360,12 @@ def dg_set_num_sms(n: int) -> None:
 
 def dg_get_num_sms() -> int:
     return int(load().dg_get_num_sms())
+
+
+def dg_set_tail_splits(n: int) -> int:
+    """Most K ranges a tile of a last, partial wave may be cut into (1: off; <= 0: default 4).
+    Returns the previous value."""
+    return int(load().dg_set_tail_splits(int(n)))
 
 
 def dg_get_device_status(stream=None) -> int:

@@ -37,6 +37,24 @@ dg_status fail_cuda(cudaError_t e, const char* what) {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 16;
+// Most K ranges a tile of a last, partial wave is cut into by the FP32-scale kernel (the kernel
+// decides per launch whether splitting pays). DG_TAIL_SPLITS sets the initial value and
+// dg_set_tail_splits() changes it; 1 switches the tail split off.
+constexpr int kTailSplits = 4;
+std::atomic<int> g_tail_splits{-1};   // -1: not yet initialised from DG_TAIL_SPLITS
+
+int clamp_tail_splits(int x) { return x < 1 ? 1 : (x > kMaxSplits ? kMaxSplits : x); }
+
+int tail_splits_setting() {
+  int v = g_tail_splits.load();
+  if (v < 0) {
+    const char* e = std::getenv("DG_TAIL_SPLITS");
+    int expected = -1;
+    g_tail_splits.compare_exchange_strong(expected, clamp_tail_splits(e ? std::atoi(e) : kTailSplits));
+    v = g_tail_splits.load();
+  }
+  return v;
+}
 
 struct DeviceState {
   bool ready = false;
@@ -335,8 +353,12 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.flags = (a_mn ? dg::kFlagAMN : 0) | (b_mn ? dg::kFlagBMN : 0) | (accumulate ? dg::kFlagAccumulate : 0);
   p.num_splits = cfg.splits;
   p.kb_per_split = cfg.kb_per_split;
-  p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles * cfg.splits;
-  p.raster_m = cfg.raster_m;
+  p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles;   // masked: counted on the device
+  p.raster_m = (int16_t)cfg.raster_m;
+  // Tail split (FP32-scale kernel, no host split-K, not the fused SwiGLU): the workspace holds at
+  // most one wave of split units, the counters one per CTA.
+  const bool tail = !block_scaled && !swiglu && cfg.splits == 1 && tail_splits_setting() > 1;
+  p.tail_splits = (int16_t)(tail ? tail_splits_setting() : 1);
   // (the block-scaled kernel reads these as its packed UE8M0 words)
   p.sA = static_cast<const float*>(sA);
   p.sB = static_cast<const float*>(sB);
@@ -348,9 +370,11 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
     cudaError_t ce = cudaMemcpyAsync(D, C, (size_t)rows * N * sizeof(float), cudaMemcpyDeviceToDevice, stream);
     if (ce != cudaSuccess) return fail_cuda(ce, "cudaMemcpyAsync(C -> D)");
   }
-  if (cfg.splits > 1) {
-    const size_t floats = (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n;
-    if ((s = ensure_workspace(*st, floats, (size_t)cfg.tiles, stream)) != DG_OK) return s;
+  if (cfg.splits > 1 || tail) {
+    const size_t floats = cfg.splits > 1 ? (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n
+                                         : (size_t)cfg.grid * 128 * cfg.block_n;
+    const size_t counters = cfg.splits > 1 ? (size_t)cfg.tiles : (size_t)cfg.grid;
+    if ((s = ensure_workspace(*st, floats, counters, stream)) != DG_OK) return s;
     p.workspace = st->workspace;
     p.counters = st->counters;
   }
@@ -455,7 +479,8 @@ dg_status run_k_grouped(bool out_f32, const uint8_t* A, const float* sA, const u
   p.num_splits = 1;
   p.kb_per_split = p.nkb;
   p.num_tiles = tiles;
-  p.raster_m = mb < 16 ? mb : 16;
+  p.raster_m = (int16_t)(mb < 16 ? mb : 16);
+  p.tail_splits = 1;   // every group's K range comes from its offsets
   p.sA = sA;
   p.sB = sB;
   p.D = D;
@@ -653,6 +678,12 @@ void dg_set_num_sms(int n) {
   g_num_sms_cap.store(n > 0 ? n : 0);
 }
 
+int dg_set_tail_splits(int n) {
+  const int prev = tail_splits_setting();
+  g_tail_splits.store(n > 0 ? clamp_tail_splits(n) : kTailSplits);
+  return prev;
+}
+
 int dg_get_num_sms(void) {
   DeviceState* st = nullptr;
   if (device_state(&st) != DG_OK) {
@@ -818,8 +849,9 @@ extern "C" dg_status dg_fp8_gemm_nt_noalloc(const uint8_t* A, const float* sA, c
   p.num_n_blocks = ceil_div(N, cfg.block_n);
   p.num_splits = cfg.splits;
   p.kb_per_split = cfg.kb_per_split;
-  p.num_tiles = cfg.tiles * cfg.splits;
-  p.raster_m = cfg.raster_m;
+  p.num_tiles = cfg.tiles;
+  p.raster_m = (int16_t)cfg.raster_m;
+  p.tail_splits = 1;   // the fixed scratch is sized for host split-K only
   p.sA = sA;
   p.sB = sB;
   p.D = D;

@@ -60,10 +60,11 @@ struct GemmParams {
   int ldsa;          // row stride of the MN-major A scales (M or M_max rounded up to 4)
   int num_m_blocks;  // ceil(M / 128)
   int num_n_blocks;  // ceil(N / BN)
-  int num_splits;    // split-K factor
+  int num_splits;    // split-K factor of every tile (1: none; see Sched)
   int kb_per_split;  // K-blocks per split (the last split may get fewer)
-  int num_tiles;     // dense/contiguous: m_blocks * n_blocks * splits; masked: computed on device
-  int raster_m;      // m-blocks per rasterisation group
+  int num_tiles;     // output tiles (dense/contiguous/K-grouped); masked: counted on device
+  int16_t raster_m;     // m-blocks per rasterisation group
+  int16_t tail_splits;  // most K ranges a tile of a last, partial wave may be cut into (1: never)
   const float* sA;           // block-scaled kernel: the packed UE8M0 words (uint32) instead
   const float* sB;           // block-scaled kernel: the packed UE8M0 words (uint32) instead
   const int32_t* m_indices;  // K-grouped: the [G+1] K offsets of the groups (K is then K_total)
@@ -87,7 +88,8 @@ struct Tile {
   int m_blk;      // 128-row block within the group (contiguous/dense: within A)
   int n_blk;      // BN-column block
   int split;      // K split
-  int out_idx;    // index of the output tile (split-K workspace / counters)
+  int splits;     // K splits of this tile (1: computed whole)
+  int out_idx;    // index of the split tile (split-K workspace / counters)
   int a_row;      // first row of the tile in A's 2-D view (also D's)
   int rows;       // rows of the tile that exist for this group (<= 128)
   int kb0, kb1;   // K-block range
@@ -120,16 +122,74 @@ __device__ __forceinline__ int masked_total_tiles(const GemmParams& p, int lane,
   return total;
 }
 
-// Decodes linear tile id t (warp-cooperative for masked and contiguous modes).
+// Work units of the persistent loop. Output tiles [0, whole) of the linear order run whole; every
+// later tile is cut into `splits` K ranges of `kps` K-blocks, and the last range to finish reduces
+// the partial tiles (split-K). Unit ids: tiles first, then the ranges of each split tile in turn.
+struct Sched {
+  int whole;   // tiles computed whole
+  int splits;  // K ranges per remaining tile
+  int kps;     // K-blocks per range
+  int units;   // whole + (tiles - whole) * splits
+};
+
+// A host-chosen split (num_splits > 1) applies to every tile. Otherwise, with TAIL and
+// tail_splits > 1, the last partial wave (tiles % grid, at most half the grid) is split along K when
+// the K-blocks it saves outweigh the exchange. Model of the FP32-scale kernel on GB300, in ns: a
+// K-block 534; publishing a partial 2500 (BN=256) / 1600 (BN=128); reducing, per split, 1000 / 600.
+template <int BN, bool TAIL>
+__device__ __forceinline__ Sched make_sched(const GemmParams& p, int tiles, int grid) {
+  Sched s;
+  if (p.num_splits > 1) {
+    s.whole = 0;
+    s.splits = p.num_splits;
+    s.kps = p.kb_per_split;
+  } else {
+    s.whole = tiles;
+    s.splits = 1;
+    s.kps = p.nkb;
+    const int rem = tiles % grid;
+    if (TAIL && p.tail_splits > 1 && rem > 0 && 2 * rem <= grid) {
+      constexpr int kPub = BN == 256 ? 2500 : 1600, kRed = BN == 256 ? 1000 : 600, kKb = 534;
+      int best_gain = 0;
+      for (int S = 2; S <= p.tail_splits && S * rem <= grid; ++S) {
+        const int kps = (p.nkb + S - 1) / S;
+        const int eff = (p.nkb + kps - 1) / kps;   // ranges that are not empty
+        const int gain = (p.nkb - kps) * kKb - (kPub + eff * kRed);
+        if (eff > 1 && gain > best_gain) {
+          best_gain = gain;
+          s.whole = tiles - rem;
+          s.splits = eff;
+          s.kps = kps;
+        }
+      }
+    }
+  }
+  s.units = s.whole + (tiles - s.whole) * s.splits;
+  return s;
+}
+
+// Decodes work unit t (warp-cooperative for masked and contiguous modes).
 template <int BN, Mode MODE>
-__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, int lane) {
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Sched& sc, int t, int lane) {
   Tile tile;
   tile.skip = false;
-  tile.split = t % p.num_splits;
-  const int u = t / p.num_splits;
-  tile.out_idx = u;
-  tile.kb0 = tile.split * p.kb_per_split;
-  tile.kb1 = min(p.nkb, tile.kb0 + p.kb_per_split);
+  int u;   // output tile
+  if (t < sc.whole) {
+    u = t;
+    tile.split = 0;
+    tile.splits = 1;
+    tile.out_idx = 0;
+    tile.kb0 = 0;
+    tile.kb1 = p.nkb;
+  } else {
+    const int v = t - sc.whole;
+    u = sc.whole + v / sc.splits;
+    tile.split = v % sc.splits;
+    tile.splits = sc.splits;
+    tile.out_idx = u - sc.whole;
+    tile.kb0 = tile.split * sc.kps;
+    tile.kb1 = min(p.nkb, tile.kb0 + sc.kps);
+  }
   if (tile.kb1 <= tile.kb0) tile.skip = true;
   if constexpr (MODE == kMasked) {
     // u -> (g, m_blk, n_blk): groups in order, within a group m fastest so the (at most two for
@@ -339,6 +399,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Plan::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 8);
+  volatile int* sched_smem = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 16);   // Sched, 4 ints
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -362,6 +423,19 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     *last_flag = 0;
     fence_barrier_init();
   }
+  if (warp == 0) {
+    // the launch's work units, the same in every CTA (masked: tiles counted from masked_m)
+    int tiles = p.num_tiles;
+    if constexpr (MODE == kMasked) tiles = masked_total_tiles(p, lane, blockIdx.x == 0);
+    const Sched sc = make_sched<BN, true>(p, tiles, (int)gridDim.x);
+    if (lane == 0) {
+      sched_smem[0] = sc.whole; sched_smem[1] = sc.splits; sched_smem[2] = sc.kps; sched_smem[3] = sc.units;
+    }
+    if (lane < kEpiWarps) {   // and in ints 8..11 of every epilogue warp's stash
+      volatile int* st = reinterpret_cast<volatile int*>(smem + Plan::kStashOff + lane * 64);
+      st[8] = sc.whole; st[9] = sc.splits; st[10] = sc.kps; st[11] = sc.units;
+    }
+  }
   if (warp == R::kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -379,11 +453,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   if (warp >= kEpiWarps) {
     // ================================================================== producer / MMA warpgroup
     if constexpr (R::kRebalance) setmaxnreg_dec<R::kOtherRegs>();
-    int total_tiles = p.num_tiles;
-    if constexpr (MODE == kMasked) {
-      if (warp <= R::kMmaWarp)
-        total_tiles = masked_total_tiles(p, lane, blockIdx.x == 0 && warp == R::kProducerWarp) * p.num_splits;
-    }
+    const Sched sc = {sched_smem[0], sched_smem[1], sched_smem[2], sched_smem[3]};
+    const int total_units = sc.units;
     if (warp == R::kProducerWarp) {
       // ---------------------------------------------------------------- TMA producer
       uint32_t it = 0;
@@ -392,8 +463,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
       const uint64_t policy = l2_policy_evict_last();
-      for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
-        const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+      for (int t = blockIdx.x; alive && t < total_units; t += gridDim.x) {
+        const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
         const int b_row = (MODE == kKGrouped ? 0 : tile.g * p.N) + tile.n_blk * BN;
         // Lane 0 runs the tile's K loop on its own (no warp-wide step per K-block).
@@ -447,8 +518,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       bool alive = true;
       int last_b = -1;
       uint32_t last_ph = 0;
-      for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
-        const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+      for (int t = blockIdx.x; alive && t < total_units; t += gridDim.x) {
+        const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
         // Lane 0 runs the tile's K loop on its own (no warp-wide step per K-block).
         int ok = 1;
@@ -496,12 +567,11 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   } else {
     // ================================================================== epilogue warpgroups
     if constexpr (R::kRebalance) setmaxnreg_inc<R::kEpiRegs>();
-    int total_tiles = p.num_tiles;
-    if constexpr (MODE == kMasked) total_tiles = masked_total_tiles(p, lane, false) * p.num_splits;
     const int quad = warp % 4;              // TMEM lanes 32*quad .. 32*quad+31
     const int cgrp = warp / 4;              // columns EPI_COLS*cgrp .. of the tile
     // The tile description is parked in shared memory across the K loop, so that only the loop's
-    // own values occupy registers next to the 128 accumulators and the 64 loaded partials.
+    // own values occupy registers next to the 128 accumulators and the 64 loaded partials. Ints
+    // 8..11 hold the launch's Sched (whole, splits, kps, units), read where needed.
     volatile int* stash = reinterpret_cast<volatile int*>(smem + Plan::kStashOff + warp * 64);
     const int row_in_tile = quad * 32 + lane;
     uint8_t* staging = smem + Plan::kStagingOff + warp * Plan::kStagingPerWarp;
@@ -514,14 +584,15 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     float2 acc2[EPI_COLS / 2];
     float* const acc = reinterpret_cast<float*>(acc2);
 
-    for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; alive && t < stash[11]; t += gridDim.x) {
       int kb_begin, kb_end;
       {
-        const Tile tile0 = decode_tile<BN, MODE>(p, t, lane);
+        const Sched sc = {stash[8], stash[9], stash[10], stash[11]};
+        const Tile tile0 = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile0.skip) continue;
         if (lane == 0) {
           stash[0] = tile0.g; stash[1] = tile0.m_blk; stash[2] = tile0.n_blk; stash[3] = tile0.split;
-          stash[4] = tile0.out_idx; stash[5] = tile0.a_row; stash[6] = tile0.rows;
+          stash[4] = tile0.out_idx; stash[5] = tile0.a_row; stash[6] = tile0.rows; stash[7] = tile0.splits;
         }
         kb_begin = tile0.kb0;
         kb_end = tile0.kb1;
@@ -598,11 +669,11 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       }
       if (!alive) break;
       // the rest of the tile description, back from shared memory
-      tile.split = stash[3]; tile.out_idx = stash[4]; tile.a_row = stash[5];
+      tile.split = stash[3]; tile.out_idx = stash[4]; tile.a_row = stash[5]; tile.splits = stash[7];
 
       // ---------------- split-K: publish the partial, and let the last split reduce
-      if (p.num_splits > 1) {
-        float* ws_tile = p.workspace + (size_t)tile.out_idx * p.num_splits * (128 * BN);
+      if (tile.splits > 1) {
+        float* ws_tile = p.workspace + (size_t)tile.out_idx * tile.splits * (128 * BN);
         float* mine = ws_tile + (size_t)tile.split * (128 * BN);
         if (row_exists && col_exists) {
           // layout [column/4][row][4]: a warp's float4 stores are 512 contiguous bytes
@@ -621,7 +692,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           ok = mbar_wait(epi_arrive_bar, sk_it & 1, abort_flag, p.status);
           if (ok) {
             const int prev = atomicAdd(p.counters + tile.out_idx, 1);
-            const int last = (prev == p.num_splits - 1);
+            const int last = (prev == tile.splits - 1);
             if (last) p.counters[tile.out_idx] = 0;   // ready for the next call
             *last_flag = last;
             mbar_arrive(epi_release_bar);
@@ -638,7 +709,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           // total = partial_0 + partial_1 + ... in split order, whichever split arrived last
 #pragma unroll
           for (int i = 0; i < EPI_COLS; ++i) acc[i] = 0.0f;
-          for (int sp = 0; sp < p.num_splits; ++sp) {
+          for (int sp = 0; sp < tile.splits; ++sp) {
             const float* src = ws_tile + (size_t)sp * (128 * BN);
 #pragma unroll
             for (int j = 0; j < EPI_COLS; j += 4) {

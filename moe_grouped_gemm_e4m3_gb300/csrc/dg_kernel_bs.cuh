@@ -154,11 +154,13 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
   if (warp >= R::kEpiWarps) {
     // ================================================================== scale / producer / MMA
     setmaxnreg_dec<R::kOtherRegs>();
-    int total_tiles = p.num_tiles;
+    int tiles = p.num_tiles;
     if constexpr (MODE == kMasked) {
-      if (warp <= R::kMmaWarp)
-        total_tiles = masked_total_tiles(p, lane, blockIdx.x == 0 && warp == R::kProducerWarp) * p.num_splits;
+      if (warp <= R::kMmaWarp) tiles = masked_total_tiles(p, lane, blockIdx.x == 0 && warp == R::kProducerWarp);
     }
+    // every tile is split the same way here (num_splits); no tail split in this kernel
+    const Sched sc = make_sched<BN, false>(p, tiles, (int)gridDim.x);
+    const int total_tiles = sc.units;
     if (warp == R::kProducerWarp) {
       // ---------------------------------------------------------------- TMA producer
       uint32_t it = 0;
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
       const uint64_t policy = l2_policy_evict_last();
       for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
-        const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+        const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
         const int b_row = tile.g * p.N + tile.n_blk * BN;
         int ok = 1;
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       uint32_t it = 0, sf_it = 0, tile_it = 0;
       bool alive = true, issued_any = false;
       for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
-        const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+        const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
         int ok = 1;
         if (lane == 0) {
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         return true;
       };
       for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
-        const Tile tile = decode_tile<BN, MODE>(p, t, lane);
+        const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
         if (poster && !post(tile, 0)) { alive = false; break; }
         const int row_in_tile = q * 32 + lane;
