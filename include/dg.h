@@ -281,8 +281,9 @@ int dg_get_mk_alignment_for_contiguous_layout(void);
 void dg_set_num_sms(int n);
 int dg_get_num_sms(void);
 
-/* Tail split of the FP32-scale kernels (dense, contiguous and masked forms, not the fused SwiGLU;
-   calls whose configuration already splits K are unaffected). When the output tiles of a launch
+/* Tail split of the dense, contiguous and masked forms, with either scale form (not the fused
+   SwiGLU, the K-grouped form or dg_fp8_gemm_nt_noalloc; calls whose configuration already splits K
+   are unaffected). When the output tiles of a launch
    leave a last, partial wave of at most half the grid, the kernel may cut each of those tiles into
    up to n K ranges, computed by otherwise idle SMs and summed in range order (deterministic) by the
    last range to finish, exactly as split-K does. The kernel takes the split only when its cost model

@@ -37,8 +37,8 @@ dg_status fail_cuda(cudaError_t e, const char* what) {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 16;
-// Most K ranges a tile of a last, partial wave is cut into by the FP32-scale kernel (the kernel
-// decides per launch whether splitting pays). DG_TAIL_SPLITS sets the initial value and
+// Most K ranges a tile of a last, partial wave is cut into (the kernel decides per launch whether
+// splitting pays). DG_TAIL_SPLITS sets the initial value and
 // dg_set_tail_splits() changes it; 1 switches the tail split off.
 constexpr int kTailSplits = 4;
 std::atomic<int> g_tail_splits{-1};   // -1: not yet initialised from DG_TAIL_SPLITS
@@ -355,9 +355,9 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles;   // masked: counted on the device
   p.raster_m = (int16_t)cfg.raster_m;
-  // Tail split (FP32-scale kernel, no host split-K, not the fused SwiGLU): the workspace holds at
-  // most one wave of split units, the counters one per CTA.
-  const bool tail = !block_scaled && !swiglu && cfg.splits == 1 && tail_splits_setting() > 1;
+  // Tail split (no host split-K, not the fused SwiGLU): the workspace holds at most one wave of
+  // split units, the counters one per CTA.
+  const bool tail = !swiglu && cfg.splits == 1 && tail_splits_setting() > 1;
   p.tail_splits = (int16_t)(tail ? tail_splits_setting() : 1);
   // (the block-scaled kernel reads these as its packed UE8M0 words)
   p.sA = static_cast<const float*>(sA);

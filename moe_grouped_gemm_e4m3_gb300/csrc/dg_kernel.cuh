@@ -134,9 +134,10 @@ struct Sched {
 
 // A host-chosen split (num_splits > 1) applies to every tile. Otherwise, with TAIL and
 // tail_splits > 1, the last partial wave (tiles % grid, at most half the grid) is split along K when
-// the K-blocks it saves outweigh the exchange. Model of the FP32-scale kernel on GB300, in ns: a
-// K-block 534; publishing a partial 2500 (BN=256) / 1600 (BN=128); reducing, per split, 1000 / 600.
-template <int BN, bool TAIL>
+// the K-blocks it saves outweigh the exchange. Model on GB300, in ns: a K-block KB_NS (534 with
+// CUDA-core promotion, 300 block-scaled); publishing a partial 2500 (BN=256) / 1600 (BN=128);
+// reducing, per split, 1000 / 600.
+template <int BN, bool TAIL, int KB_NS>
 __device__ __forceinline__ Sched make_sched(const GemmParams& p, int tiles, int grid) {
   Sched s;
   if (p.num_splits > 1) {
@@ -149,7 +150,7 @@ __device__ __forceinline__ Sched make_sched(const GemmParams& p, int tiles, int 
     s.kps = p.nkb;
     const int rem = tiles % grid;
     if (TAIL && p.tail_splits > 1 && rem > 0 && 2 * rem <= grid) {
-      constexpr int kPub = BN == 256 ? 2500 : 1600, kRed = BN == 256 ? 1000 : 600, kKb = 534;
+      constexpr int kPub = BN == 256 ? 2500 : 1600, kRed = BN == 256 ? 1000 : 600, kKb = KB_NS;
       int best_gain = 0;
       for (int S = 2; S <= p.tail_splits && S * rem <= grid; ++S) {
         const int kps = (p.nkb + S - 1) / S;
@@ -427,7 +428,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     // the launch's work units, the same in every CTA (masked: tiles counted from masked_m)
     int tiles = p.num_tiles;
     if constexpr (MODE == kMasked) tiles = masked_total_tiles(p, lane, blockIdx.x == 0);
-    const Sched sc = make_sched<BN, true>(p, tiles, (int)gridDim.x);
+    const Sched sc = make_sched<BN, true, 534>(p, tiles, (int)gridDim.x);
     if (lane == 0) {
       sched_smem[0] = sc.whole; sched_smem[1] = sc.splits; sched_smem[2] = sc.kps; sched_smem[3] = sc.units;
     }

@@ -158,8 +158,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
     if constexpr (MODE == kMasked) {
       if (warp <= R::kMmaWarp) tiles = masked_total_tiles(p, lane, blockIdx.x == 0 && warp == R::kProducerWarp);
     }
-    // every tile is split the same way here (num_splits); no tail split in this kernel
-    const Sched sc = make_sched<BN, false>(p, tiles, (int)gridDim.x);
+    const Sched sc = make_sched<BN, true, 300>(p, tiles, (int)gridDim.x);
     const int total_tiles = sc.units;
     if (warp == R::kProducerWarp) {
       // ---------------------------------------------------------------- TMA producer
@@ -277,7 +276,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
           return false;
         if (lane == 0) {
           volatile int* d = desc_ring + ds * 8;
-          d[0] = tl.g; d[1] = tl.m_blk; d[2] = tl.n_blk; d[3] = tl.split;
+          d[0] = tl.g; d[1] = tl.m_blk; d[2] = tl.n_blk; d[3] = tl.split | (tl.splits << 16);
           d[4] = tl.out_idx; d[5] = tl.a_row; d[6] = tl.rows; d[7] = end;
           mbar_arrive(&desc_full_bar[ds]);
         }
@@ -319,6 +318,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       if (poster && alive) {
         Tile end_mark;
         end_mark.g = end_mark.m_blk = end_mark.n_blk = end_mark.split = end_mark.out_idx = 0;
+        end_mark.splits = 1;
         end_mark.a_row = end_mark.rows = 0;
         post(end_mark, 1);
       }
@@ -382,7 +382,8 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty_bar);
       Tile tile;
-      tile.g = stash[0]; tile.m_blk = stash[1]; tile.n_blk = stash[2]; tile.split = stash[3];
+      tile.g = stash[0]; tile.m_blk = stash[1]; tile.n_blk = stash[2];
+      tile.split = stash[3] & 0xFFFF; tile.splits = stash[3] >> 16;   // (split, splits) packed in one int
       tile.out_idx = stash[4]; tile.a_row = stash[5]; tile.rows = stash[6];
       const int m_local = tile.m_blk * 128 + row_in_tile;
       const bool row_exists = row_in_tile < tile.rows;
@@ -390,8 +391,8 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       const bool col_exists = n_col0 < p.N;
 
       // ---------------- split-K: publish the partial, and let the last split reduce
-      if (p.num_splits > 1) {
-        float* ws_tile = p.workspace + (size_t)tile.out_idx * p.num_splits * (128 * BN);
+      if (tile.splits > 1) {
+        float* ws_tile = p.workspace + (size_t)tile.out_idx * tile.splits * (128 * BN);
         float* mine = ws_tile + (size_t)tile.split * (128 * BN);
         if (row_exists && col_exists) {
 #pragma unroll
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
           ok = mbar_wait(epi_arrive_bar, sk_it & 1, abort_flag, p.status);
           if (ok) {
             const int prev = atomicAdd(p.counters + tile.out_idx, 1);
-            const int last = (prev == p.num_splits - 1);
+            const int last = (prev == tile.splits - 1);
             if (last) p.counters[tile.out_idx] = 0;   // ready for the next call
             *last_flag = last;
             mbar_arrive(epi_release_bar);
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
           // total = partial_0 + partial_1 + ... in split order, whichever split arrived last
 #pragma unroll
           for (int i = 0; i < EPI_COLS; ++i) acc[i] = 0.0f;
-          for (int sp = 0; sp < p.num_splits; ++sp) {
+          for (int sp = 0; sp < tile.splits; ++sp) {
             const float* src = ws_tile + (size_t)sp * (128 * BN);
 #pragma unroll
             for (int j = 0; j < EPI_COLS; j += 4) {

@@ -1,4 +1,4 @@
-"""GPU parity of the tail split (FP32-scale kernel): the tiles of a last, partial wave cut along K.
+"""GPU parity of the tail split: the tiles of a last, partial wave cut along K (both kernels).
 
 Each case runs the same call with the tail split on (default) and off (dg_set_tail_splits(1)) and
 checks:
@@ -31,12 +31,15 @@ def dg():
     assert m.dg_get_device_status() == 0
 
 
-def _tail(tiles, grid, nkb, bn, max_splits=4):
+KB_NS = {"fp32": 534, "ue8m0": 300}   # the kernels' cost of one K-block in their tail-split model
+
+
+def _tail(tiles, grid, nkb, bn, kb_ns=534, max_splits=4):
     """(first tail tile, K ranges per tail tile) under the kernel's rule; (tiles, 1) if none."""
     rem = tiles % grid
     if not (max_splits > 1 and rem > 0 and 2 * rem <= grid):
         return tiles, 1
-    pub, red, kb = (2500, 1000, 534) if bn == 256 else (1600, 600, 534)
+    pub, red, kb = (2500, 1000, kb_ns) if bn == 256 else (1600, 600, kb_ns)
     best, out = 0, (tiles, 1)
     s = 2
     while s <= max_splits and s * rem <= grid:
@@ -78,23 +81,38 @@ def _dense_shape(dg):
     return 128 * mb, 256 * nb, 4096
 
 
-def test_tail_split_dense(dg):
+def _scales(a, b, scales):
+    """(device sA, device sB, oracle sA, oracle sB): FP32 scales, or packed UE8M0 words and the
+    FP32 scales the oracle decodes from those words."""
+    if scales == "fp32":
+        return a.sA, b.sB, a.sA, b.sB
+    nkb = -(-a.A.shape[-1] // 128)
+    pa, pb = dg_inputs.pack_ue8m0_a(a.sA), dg_inputs.pack_ue8m0_b(b.sB)
+    return pa, pb, oracle.unpack_ue8m0_a(pa, nkb), oracle.unpack_ue8m0_b(pb, nkb)
+
+
+@pytest.mark.parametrize("scales", ["fp32", "ue8m0"])
+def test_tail_split_dense(dg, scales):
+    ue = scales == "ue8m0"
     M, N, K = _dense_shape(dg)
-    cfg = dg.dg_query_config(0, M, N, K)
+    cfg = (dg.dg_query_config_ue8m0 if ue else dg.dg_query_config)(0, M, N, K)
     assert cfg["splits"] == 1 and cfg["block_n"] == 256
     mb, nb = M // 128, N // 256
     tiles = mb * nb
-    first, splits = _tail(tiles, cfg["grid"], K // 128, 256)
+    first, splits = _tail(tiles, cfg["grid"], K // 128, 256, KB_NS[scales])
     assert splits > 1, f"expected a tail split: tiles={tiles} grid={cfg['grid']}"
-    a = dg_inputs.make_a(M, K, seed=41)
-    b = dg_inputs.make_b(1, N, K, seed=41)
-    A, sA, B, sB = dev(a.A), dev(a.sA), dev(b.B[0]), dev(b.sB[0])
+    a = dg_inputs.make_a(M, K, seed=41, ue8m0=ue)
+    b = dg_inputs.make_b(1, N, K, seed=41, ue8m0=ue)
+    gsA, gsB, osA, osB = _scales(a, b, scales)
+    A, sA, B, sB = dev(a.A), dev(gsA), dev(b.B[0]), dev(gsB[0])
+    f_bf16 = dg.dg_fp8_gemm_nt_ue8m0 if ue else dg.dg_fp8_gemm_nt
+    f_f32 = dg.dg_fp8_gemm_nt_ue8m0_f32 if ue else dg.dg_fp8_gemm_nt_f32
 
     def run():
         D = bf16_sentinel((M, N))
         D32 = f32_sentinel((M, N))
-        dg.dg_fp8_gemm_nt(A, sA, B, sB, D)
-        dg.dg_fp8_gemm_nt_f32(A, sA, B, sB, D32)
+        f_bf16(A, sA, B, sB, D)
+        f_f32(A, sA, B, sB, D32)
         torch.cuda.synchronize()
         return bits16(D).cpu(), D32.cpu().numpy()
 
@@ -114,9 +132,9 @@ def test_tail_split_dense(dg):
     pick = rng.choice(len(tm), 1500, replace=False)
     ms = np.concatenate([tm[pick], rng.integers(0, M, 500)])
     ns = np.concatenate([tn[pick], rng.integers(0, N, 500)])
-    ref = oracle.gemm_nt_sampled(a.A, a.sA, b.B[0], b.sB[0], ms, ns)
-    assert_accurate(f_on[ms, ns], d_on.numpy()[ms, ns], ref, "tail split on")
-    assert_accurate(f_off[ms, ns], d_off.numpy()[ms, ns], ref, "tail split off")
+    ref = oracle.gemm_nt_sampled(a.A, osA, b.B[0], osB[0], ms, ns)
+    assert_accurate(f_on[ms, ns], d_on.numpy()[ms, ns], ref, f"{scales} tail split on")
+    assert_accurate(f_off[ms, ns], d_off.numpy()[ms, ns], ref, f"{scales} tail split off")
 
 
 def test_tail_split_contiguous_with_padding(dg):
@@ -161,26 +179,31 @@ def test_tail_split_contiguous_with_padding(dg):
         assert_accurate(d, bits, ref, f"contiguous tail split {what}")
 
 
-def test_tail_split_masked_decode(dg):
+@pytest.mark.parametrize("scales", ["fp32", "ue8m0"])
+def test_tail_split_masked_decode(dg, scales):
     # the decode shape: 16 groups, masked_m from seed 0, N=4096, K=7168 (320 tiles: a tail of 16)
+    ue = scales == "ue8m0"
     G, M_max, N, K = 16, 256, 4096, 7168
     masked_m = dg_inputs.make_masked_m(G, M_max, seed=0)
     mbs = [-(-int(m) // 128) for m in masked_m]
     nb = N // 256
     tiles = sum(mbs) * nb
-    grid = dg.dg_query_config(2, M_max, N, K, G)["grid"]
-    first, splits = _tail(tiles, grid, K // 128, 256)
+    grid = (dg.dg_query_config_ue8m0 if ue else dg.dg_query_config)(2, M_max, N, K, G)["grid"]
+    first, splits = _tail(tiles, grid, K // 128, 256, KB_NS[scales])
     if splits == 1:
         pytest.skip(f"no tail split for tiles={tiles} on grid={grid}")
-    a = dg_inputs.make_masked_a(G, M_max, K, seed=0)
-    b = dg_inputs.make_b(G, N, K, seed=0)
-    A, sA, B, sB, MM = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(masked_m)
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=0, ue8m0=ue)
+    b = dg_inputs.make_b(G, N, K, seed=0, ue8m0=ue)
+    gsA, gsB, osA, osB = _scales(a, b, scales)
+    A, sA, B, sB, MM = dev(a.A), dev(gsA), dev(b.B), dev(gsB), dev(masked_m)
+    f_bf16 = dg.dg_fp8_grouped_masked_ue8m0 if ue else dg.dg_fp8_grouped_masked
+    f_f32 = dg.dg_fp8_grouped_masked_ue8m0_f32 if ue else dg.dg_fp8_grouped_masked_f32
 
     def run():
         D = bf16_sentinel((G, M_max, N))
         D32 = f32_sentinel((G, M_max, N))
-        dg.dg_fp8_grouped_masked(A, sA, B, sB, MM, D)
-        dg.dg_fp8_grouped_masked_f32(A, sA, B, sB, MM, D32)
+        f_bf16(A, sA, B, sB, MM, D)
+        f_f32(A, sA, B, sB, MM, D32)
         torch.cuda.synchronize()
         return bits16(D).cpu(), D32.cpu().numpy()
 
@@ -208,9 +231,9 @@ def test_tail_split_masked_decode(dg):
     gs, ms, ns = np.nonzero(sel_tail)
     pick = rng.choice(len(gs), 1500, replace=False)
     gs, ms, ns = gs[pick], ms[pick], ns[pick]
-    ref = oracle.masked_sampled(a.A, a.sA, b.B, b.sB, gs, ms, ns)
-    assert_accurate(f_on[gs, ms, ns], d_on.numpy()[gs, ms, ns], ref, "masked tail split on")
-    assert_accurate(f_off[gs, ms, ns], d_off.numpy()[gs, ms, ns], ref, "masked tail split off")
+    ref = oracle.masked_sampled(a.A, osA, b.B, osB, gs, ms, ns)
+    assert_accurate(f_on[gs, ms, ns], d_on.numpy()[gs, ms, ns], ref, f"{scales} masked tail split on")
+    assert_accurate(f_off[gs, ms, ns], d_off.numpy()[gs, ms, ns], ref, f"{scales} masked tail split off")
 
 
 def test_tail_split_setting_round_trip(dg):
@@ -221,3 +244,37 @@ def test_tail_split_setting_round_trip(dg):
         assert dg.dg_set_tail_splits(prev) == 4        # 0 restored the default
     finally:
         dg.dg_set_tail_splits(prev)
+
+
+@pytest.mark.parametrize("layout", ["nn", "tt"])
+def test_tail_split_layouts_match_nt(dg, layout):
+    # the transposed layouts take the same schedule: bitwise equal to the NT call, tail included
+    M, N, K = _dense_shape(dg)
+    a = dg_inputs.make_a(M, K, seed=44)
+    b = dg_inputs.make_b(1, N, K, seed=44)
+    sA, sB = dev(a.sA), dev(b.sB[0])
+    a_t, b_t = {"nn": (False, True), "tt": (True, False)}[layout]   # A stored [K,M] / B stored [K,N]
+    A = dev(np.ascontiguousarray(a.A.T)) if a_t else dev(a.A)
+    B = dev(np.ascontiguousarray(b.B[0].T)) if b_t else dev(b.B[0])
+    D32 = f32_sentinel((M, N))
+    getattr(dg, f"dg_fp8_gemm_{layout}_f32")(A, sA, B, sB, D32, M, N, K)
+    Dnt = f32_sentinel((M, N))
+    dg.dg_fp8_gemm_nt_f32(dev(a.A), sA, dev(b.B[0]), sB, Dnt)
+    torch.cuda.synchronize()
+    assert torch.equal(D32.view(torch.int32), Dnt.view(torch.int32))
+
+
+def test_tail_split_accumulate(dg):
+    # D = C + A·Bᵀ: the split tiles are reduced once, then added onto C once
+    M, N, K = _dense_shape(dg)
+    a = dg_inputs.make_a(M, K, seed=45)
+    b = dg_inputs.make_b(1, N, K, seed=45)
+    A, sA, B, sB = dev(a.A), dev(a.sA), dev(b.B[0]), dev(b.sB[0])
+    C = dg_inputs.draw(45, 6, M * N).reshape(M, N) * np.float32(30.0)
+    D32 = torch.full((M, N), float("nan"), device="cuda")
+    dg.dg_fp8_gemm_nt_f32(A, sA, B, sB, D32)
+    Ct = dev(C)
+    dg.dg_fp8_gemm_nt_acc_f32(A, sA, B, sB, Ct, Ct)
+    torch.cuda.synchronize()
+    want = (C.astype(np.float32) + D32.cpu().numpy()).astype(np.float32)
+    assert np.array_equal(Ct.cpu().numpy().view(np.int32), want.view(np.int32))
