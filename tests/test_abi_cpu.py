@@ -90,3 +90,15 @@ def test_build_is_up_to_date_after_load():
     from moe_grouped_gemm_e4m3_gb300 import build
     dg.load()
     assert build.up_to_date()
+
+
+def test_tail_split_setting_is_host_state():
+    # no CUDA call: the setting is read by the host when a GEMM is launched
+    prev = dg.dg_set_tail_splits(3)
+    try:
+        assert dg.dg_set_tail_splits(1) == 3          # 1: off
+        assert dg.dg_set_tail_splits(40) == 1         # clamped to 16
+        assert dg.dg_set_tail_splits(-5) == 16        # <= 0: the default, 4
+        assert dg.dg_set_tail_splits(prev) == 4
+    finally:
+        dg.dg_set_tail_splits(prev)
