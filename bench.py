@@ -81,6 +81,8 @@ def parse_args():
     ap.add_argument("--all-configs", action="store_true",
                     help="time every workload configuration (dense small, sweep, contiguous, masked, stress) "
                          "and print one JSON line per shape instead of the benchmark line")
+    ap.add_argument("--configs", default=None,
+                    help="with --all-configs: only these configuration numbers (comma-separated), e.g. 4")
     ap.add_argument("--shapes", default=None,
                     help="restrict the sweep to these MxNxK shapes (comma-separated), e.g. for profiling")
     ap.add_argument("--scales", choices=["fp32", "ue8m0"], default="fp32",
@@ -621,6 +623,8 @@ def run_all_configs(args):
         print(json.dumps(line), flush=True)
 
     scales = {"scales": "ue8m0" if UE8M0 else "fp32"}
+    chosen = None if args.configs is None else {int(c) for c in args.configs.split(",")}
+    want = lambda n: chosen is None or n in chosen
 
     def dense(config, M, N, K, dist=dg_inputs.NORMAL, outliers=0.0):
         a = dg_inputs.make_a(M, K, seed=0, dist=dist, outlier_frac=outliers, ue8m0=UE8M0)
@@ -633,10 +637,11 @@ def run_all_configs(args):
         report(config, f"{M}x{N}x{K}", 2.0 * M * N * K, algorithmic_bytes(M, N, K), ms,
                dict(scales, cfg=query_config(dg, 0, M, N, K)))
 
-    dense("1 dense small", 128, 512, 1024)
-    for (M, N, K) in [(M, N, K) for M in SWEEP_M for (N, K) in SWEEP_NK]:
+    if want(1):
+        dense("1 dense small", 128, 512, 1024)
+    for (M, N, K) in [(M, N, K) for M in SWEEP_M for (N, K) in SWEEP_NK] if want(2) else []:
         dense("2 dense sweep", M, N, K)
-    for G in (4, 8):
+    for G in (4, 8) if want(3) else ():
         for (N, K) in ((4096, 7168), (7168, 2048)):
             M = G * 8192
             a = dg_inputs.make_a(M, K, seed=0, ue8m0=UE8M0)
@@ -653,7 +658,7 @@ def run_all_configs(args):
             report("3 contiguous", f"G={G} M={M} N={N} K={K}", 2.0 * M * N * K, nbytes, ms,
                    dict(scales, cfg=query_config(dg, 1, M, N, K, G)))
             del A, B, D
-    for (N, K) in ((4096, 7168), (7168, 2048)):
+    for (N, K) in ((4096, 7168), (7168, 2048)) if want(4) else ():
         G, M_max = 16, 256
         mm = dg_inputs.make_masked_m(G, M_max, seed=0)
         a = dg_inputs.make_masked_a(G, M_max, K, seed=0, ue8m0=UE8M0)
@@ -670,10 +675,10 @@ def run_all_configs(args):
         nbytes = valid * K + active * N * K + 4 * valid * nks + 4 * G * nnb * nks + 2 * valid * N
         report("4 masked", f"G=16 M_max=256 sum(masked_m)={valid} N={N} K={K}", 2.0 * valid * N * K, nbytes, ms,
                dict(scales, cfg=query_config(dg, 2, M_max, N, K, G)))
-    for (M, N, K) in ((4096, 2112, 7168), (4096, 576, 7168), (4096, 7168, 32768)):
+    for (M, N, K) in ((4096, 2112, 7168), (4096, 576, 7168), (4096, 7168, 32768)) if want(5) else ():
         dense("5 stress (Student-t, outliers)", M, N, K, dist=dg_inputs.STUDENT_T3, outliers=0.01)
     # the masked form fused with SwiGLU (FP32 scales only): B holds 2I rows, H has I columns
-    if not UE8M0:
+    if not UE8M0 and want(7):
         for (N2, K) in ((4096, 7168),):
             G, M_max, I = 16, 256, N2 // 2
             mm = dg_inputs.make_masked_m(G, M_max, seed=0)
@@ -690,7 +695,7 @@ def run_all_configs(args):
                    2.0 * valid * N2 * K, nbytes, ms, dict(scales))
             del A, B, H
     # the NN / TN / TT layouts (FP32 scales only): A stored [K,M] and/or B stored [K,N]
-    if not UE8M0:
+    if not UE8M0 and want(8):
         M, N, K = 4096, 7168, 2048
         a = dg_inputs.make_a(M, K, seed=0)
         b = dg_inputs.make_b(1, N, K, seed=0)
@@ -705,7 +710,7 @@ def run_all_configs(args):
                    dict(scales, cfg=query_config(dg, 0, M, N, K)))
             del A, B, D
     # the K-grouped form (weight gradients): 4 experts with 1024, 0, 2048 and 512 tokens
-    if not UE8M0:
+    if not UE8M0 and want(9):
         M, N = 2048, 7168
         off = np.array([0, 1024, 1024, 3072, 3584], np.int32)
         K = int(off[-1])
@@ -722,7 +727,7 @@ def run_all_configs(args):
                nbytes, ms, dict(scales))
         del A, B, D
     # the accumulating form D = C + A·Bᵀ (FP32 C = D, in place): C is read and D written in FP32
-    for (M, N, K) in ((4096, 7168, 16384), (4096, 7168, 2048)):
+    for (M, N, K) in ((4096, 7168, 16384), (4096, 7168, 2048)) if want(6) else ():
         a = dg_inputs.make_a(M, K, seed=0, ue8m0=UE8M0)
         b = dg_inputs.make_b(1, N, K, seed=0, ue8m0=UE8M0)
         gsA, gsB = gpu_scales(a, b)
