@@ -248,7 +248,7 @@ dg_status dg_fp8_gemm_nt_ue8m0_acc_f32(const uint8_t* A, const int32_t* sA, cons
 
 /*
  * Allocation-free dense GEMM: the same computation, arguments and result as dg_fp8_gemm_nt (the
- * same kernel, tile configuration and accumulation order), for callers that cannot let a library
+ * same kernel, tile configuration, schedule and accumulation order), for callers that cannot let a library
  * call cudaMalloc — for example a framework whose caching allocator already owns the device memory,
  * or a serving loop that must not block on the device synchronisation cudaMalloc/cudaFree may do.
  * The DeepGEMM pages have no counterpart to this call; it is an addition of this library.
@@ -258,7 +258,9 @@ dg_status dg_fp8_gemm_nt_ue8m0_acc_f32(const uint8_t* A, const int32_t* sA, cons
  *   - The first call on each device looks up that array's device address (cudaGetSymbolAddress,
  *     with the device current) and caches it; make that first call before any stream capture.
  *   - A shape whose split-K scratch would exceed the array returns DG_ERR_UNSUPPORTED with a message
- *     naming the sizes (dg_fp8_gemm_nt has no such limit). Shapes that need no split-K use no scratch.
+ *     naming the sizes (dg_fp8_gemm_nt has no such limit). Shapes that need no split-K use no scratch,
+ *     nor do shapes whose split-K runs inside thread-block clusters (dg_set_cluster_split); a tail
+ *     split (dg_set_tail_splits) needs at most one wave of partials, which the array holds.
  *   - Every call on a device shares the array and the array keeps the last call's contents; the call
  *     clears the counters it uses (an asynchronous memset on `stream`) before its kernel. Calls that
  *     overlap on the GPU (e.g. on two streams of one device) race on the array and give wrong results.
@@ -296,6 +298,16 @@ int dg_get_num_sms(void);
    The pages do not describe splitting K; the tail rule is this implementation's choice for GB300's
    152 SMs. */
 int dg_set_tail_splits(int n);
+
+/* Split-K inside thread-block clusters (dense and contiguous forms with FP32 scales). When a call
+   splits K (few output tiles) into at most 8 ranges and every tile's ranges fit on the GPU at once
+   as one cluster of CTAs, the ranges reduce through distributed shared memory: partials in each
+   CTA's shared memory, cluster barriers, sums in range order. Otherwise they go through a global
+   workspace with an arrival counter per tile. Both orders are the same, so the results are bitwise
+   equal. on = 0 forces the global workspace; on != 0 (the default) allows clusters. The environment
+   variable DG_CLUSTER_SPLIT=0 sets the initial value to off. Returns the previous value (0 or 1).
+   This is an addition of this implementation; the pages do not describe split-K. */
+int dg_set_cluster_split(int on);
 
 /* Reads and clears the device status word of the current device after synchronising `stream`.
    *code receives the DG_DEV_* bits. Returns DG_ERR_DEVICE_STATUS when a bit was set. */

@@ -45,6 +45,41 @@ std::atomic<int> g_tail_splits{-1};   // -1: not yet initialised from DG_TAIL_SP
 
 int clamp_tail_splits(int x) { return x < 1 ? 1 : (x > kMaxSplits ? kMaxSplits : x); }
 
+// Split-K inside thread-block clusters (dense and contiguous, FP32 scales): on unless
+// DG_CLUSTER_SPLIT=0 or dg_set_cluster_split(0).
+std::atomic<int> g_cluster_split{-1};
+bool cluster_split_setting() {
+  int v = g_cluster_split.load();
+  if (v < 0) {
+    const char* e = std::getenv("DG_CLUSTER_SPLIT");
+    int expected = -1;
+    g_cluster_split.compare_exchange_strong(expected, (e && std::atoi(e) == 0) ? 0 : 1);
+    v = g_cluster_split.load();
+  }
+  return v != 0;
+}
+
+// Largest cluster of the cluster split-K: the portable limit.
+constexpr int kMaxClusterSplit = 8;
+
+// Resident clusters of `splits` CTAs for an instantiation, queried once per device.
+int cluster_capacity(int mode, int block_n, bool out_f32, int splits) {
+  static std::mutex mu;
+  static int cache[kMaxDevices][2][2][2][kMaxClusterSplit + 1];
+  static bool have[kMaxDevices][2][2][2][kMaxClusterSplit + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (splits < 2 || splits > kMaxClusterSplit || (mode != dg::kDense && mode != dg::kContiguous)) return 0;
+  const int m = mode == dg::kDense ? 0 : 1, b = block_n == 256 ? 1 : 0, f = out_f32 ? 1 : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev][m][b][f][splits]) {
+    cache[dev][m][b][f][splits] = m == 0 ? dg::cluster_capacity_dense(block_n, out_f32, splits)
+                                         : dg::cluster_capacity_contiguous(block_n, out_f32, splits);
+    have[dev][m][b][f][splits] = true;
+  }
+  return cache[dev][m][b][f][splits];
+}
+
 int tail_splits_setting() {
   int v = g_tail_splits.load();
   if (v < 0) {
@@ -220,12 +255,39 @@ Config choose_config(int mode, int rows, int N, int K, int G, int num_sms, bool 
   return c;
 }
 
+// Split-K in clusters needs every tile's cluster resident at once. When the chosen split count does
+// not fit, one or two fewer splits may; take the largest that does. The exchange through
+// distributed shared memory then saves more than the longer K range of each CTA costs: on
+// 64x2112x7168, 7 splits through the global workspace versus 6 in clusters. An explicit DG_SPLITS is
+// left alone.
+void fit_cluster_splits(Config& c, int mode, int K, bool block_scaled, bool out_f32) {
+  if (block_scaled || (mode != dg::kDense && mode != dg::kContiguous) || c.splits < 3) return;
+  if (!cluster_split_setting() || std::getenv("DG_SPLITS")) return;
+  if (c.splits <= kMaxClusterSplit && cluster_capacity(mode, c.block_n, out_f32, c.splits) >= c.tiles) return;
+  const int nkb = ceil_div(K, 128);
+  for (int s = c.splits - 1; s >= 2 && s >= c.splits - 2; --s) {
+    const int kps = ceil_div(nkb, s), eff = ceil_div(nkb, kps);
+    if (eff >= 2 && eff <= kMaxClusterSplit && cluster_capacity(mode, c.block_n, out_f32, eff) >= c.tiles) {
+      c.splits = eff;
+      c.kb_per_split = kps;
+      c.grid = c.tiles * eff;
+      return;
+    }
+  }
+}
+
+// Whether a call with this configuration runs its split-K in clusters: FP32 scales, dense or
+// contiguous, 2..8 splits, one work unit per CTA, and every tile's cluster resident at once.
+bool use_cluster_split(const Config& c, int mode, bool out_f32, bool block_scaled, bool swiglu) {
+  return !block_scaled && !swiglu && (mode == dg::kDense || mode == dg::kContiguous) && c.splits > 1 &&
+         c.splits <= kMaxClusterSplit && cluster_split_setting() && c.grid == c.tiles * c.splits &&
+         cluster_capacity(mode, c.block_n, out_f32, c.splits) >= c.tiles;
+}
+
+// Read on every call (a debugging aid), so that a process can switch it on and off.
 bool print_configs() {
-  static const bool on = [] {
-    const char* e = std::getenv("DG_PRINT_CONFIGS");
-    return e && std::atoi(e) != 0;
-  }();
-  return on;
+  const char* e = std::getenv("DG_PRINT_CONFIGS");
+  return e && std::atoi(e) != 0;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -324,6 +386,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   if (s != DG_OK) return s;
   const int sms = effective_sms(*st);
   Config cfg = choose_config(mode, rows, N, K, mode == dg::kDense ? 1 : G, sms, block_scaled);
+  if (!swiglu) fit_cluster_splits(cfg, mode, K, block_scaled, out_f32);
   const int d_cols = swiglu ? N / 2 : N;   // width of D (fused SwiGLU: H has I = N/2 columns)
   if (swiglu) {
     // one tile = 128 gate rows + 128 up rows of B; no split-K
@@ -370,7 +433,14 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
     cudaError_t ce = cudaMemcpyAsync(D, C, (size_t)rows * N * sizeof(float), cudaMemcpyDeviceToDevice, stream);
     if (ce != cudaSuccess) return fail_cuda(ce, "cudaMemcpyAsync(C -> D)");
   }
-  if (cfg.splits > 1 || tail) {
+  // Split-K in clusters: the splits of a tile are one cluster of CTAs that reduce through
+  // distributed shared memory (no workspace, no counters) when every tile's cluster can be resident
+  // at once and each CTA gets exactly one work unit.
+  const bool cluster = use_cluster_split(cfg, mode, out_f32, block_scaled, swiglu);
+  if (cluster) {
+    p.flags |= dg::kFlagClusterSplit;
+    a.cluster = cfg.splits;
+  } else if (cfg.splits > 1 || tail) {
     const size_t floats = cfg.splits > 1 ? (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n
                                          : (size_t)cfg.grid * 128 * cfg.block_n;
     const size_t counters = cfg.splits > 1 ? (size_t)cfg.tiles : (size_t)cfg.grid;
@@ -410,9 +480,9 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   a.stream = stream;
   if (print_configs()) {
     static const char* names[3] = {"dense", "contiguous", "masked"};
-    std::fprintf(stderr, "[dg] %s%s%s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d grid=%d tiles=%d\n",
+    std::fprintf(stderr, "[dg] %s%s%s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d%s grid=%d tiles=%d\n",
                  names[mode], block_scaled ? "/ue8m0" : "", swiglu ? "/swiglu" : "", out_f32 ? "/f32" : "", rows, N, K,
-                 p.G, cfg.block_n, cfg.stages, cfg.splits, cfg.grid, cfg.tiles);
+                 p.G, cfg.block_n, cfg.stages, cfg.splits, cluster ? " (cluster)" : "", cfg.grid, cfg.tiles);
   }
   cudaError_t e;
   if (swiglu) {
@@ -678,6 +748,12 @@ void dg_set_num_sms(int n) {
   g_num_sms_cap.store(n > 0 ? n : 0);
 }
 
+int dg_set_cluster_split(int on) {
+  const int prev = cluster_split_setting() ? 1 : 0;
+  g_cluster_split.store(on ? 1 : 0);
+  return prev;
+}
+
 int dg_set_tail_splits(int n) {
   const int prev = tail_splits_setting();
   g_tail_splits.store(n > 0 ? clamp_tail_splits(n) : kTailSplits);
@@ -732,7 +808,8 @@ dg_status query_config(int mode, int M, int N, int K, int G, int* cfg, bool bloc
   int sms = num_sms_cap();
   if (device_state(&st) == DG_OK) sms = effective_sms(*st);
   if (sms <= 0) sms = 152;  // no device: report the GB300 configuration
-  const Config c = choose_config(mode, M, N, K, mode == 0 ? 1 : G, sms, block_scaled);
+  Config c = choose_config(mode, M, N, K, mode == 0 ? 1 : G, sms, block_scaled);
+  if (st) fit_cluster_splits(c, mode, K, block_scaled, false);
   cfg[0] = 128;
   cfg[1] = c.block_n;
   cfg[2] = c.stages;
@@ -826,10 +903,16 @@ extern "C" dg_status dg_fp8_gemm_nt_noalloc(const uint8_t* A, const float* sA, c
   void* scratch = nullptr;
   if ((s = noalloc_scratch(&scratch)) != DG_OK) return s;
 
-  const Config cfg = choose_config(dg::kDense, M, N, K, 1, effective_sms(*st));
-  const size_t counter_bytes = (size_t)cfg.tiles * sizeof(int);
-  const size_t partial_bytes = (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n * sizeof(float);
-  if (cfg.splits > 1 && (counter_bytes > kNoAllocCounterBytes || partial_bytes > kNoAllocWorkspaceBytes))
+  // The schedule of dg_fp8_gemm_nt: the same configuration, cluster split-K (which needs no
+  // scratch) and the tail split (one wave of partials at most), so that the two agree bit for bit.
+  Config cfg = choose_config(dg::kDense, M, N, K, 1, effective_sms(*st));
+  fit_cluster_splits(cfg, dg::kDense, K, false, false);
+  const bool cluster = use_cluster_split(cfg, dg::kDense, false, false, false);
+  const bool tail = !cluster && cfg.splits == 1 && tail_splits_setting() > 1;
+  const bool global_split = !cluster && cfg.splits > 1;
+  const size_t counter_bytes = (size_t)(tail ? cfg.grid : cfg.tiles) * sizeof(int);
+  const size_t partial_bytes = (size_t)(tail ? cfg.grid : cfg.tiles * cfg.splits) * 128 * cfg.block_n * sizeof(float);
+  if ((global_split || tail) && (counter_bytes > kNoAllocCounterBytes || partial_bytes > kNoAllocWorkspaceBytes))
     return fail(DG_ERR_UNSUPPORTED,
                 "dg_fp8_gemm_nt_noalloc: this shape needs " + std::to_string(partial_bytes) + " bytes of split-K "
                 "partials and " + std::to_string(cfg.tiles) + " counters; the fixed scratch holds " +
@@ -851,12 +934,15 @@ extern "C" dg_status dg_fp8_gemm_nt_noalloc(const uint8_t* A, const float* sA, c
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = cfg.tiles;
   p.raster_m = (int16_t)cfg.raster_m;
-  p.tail_splits = 1;   // the fixed scratch is sized for host split-K only
+  p.tail_splits = (int16_t)(tail ? tail_splits_setting() : 1);
   p.sA = sA;
   p.sB = sB;
   p.D = D;
   p.status = st->status;
-  if (cfg.splits > 1) {
+  if (cluster) {
+    p.flags |= dg::kFlagClusterSplit;
+    a.cluster = cfg.splits;
+  } else if (global_split || tail) {
     unsigned char* base = static_cast<unsigned char*>(scratch);
     p.counters = reinterpret_cast<int*>(base);
     p.workspace = reinterpret_cast<float*>(base + kNoAllocCounterBytes);

@@ -3,4 +3,7 @@
 
 namespace dg {
 cudaError_t launch_contiguous(const LaunchArgs& a) { return launch_mode<kContiguous>(a); }
+int cluster_capacity_contiguous(int block_n, bool out_f32, int cluster) {
+  return cluster_capacity_mode<kContiguous>(block_n, out_f32, cluster);
+}
 }  // namespace dg

@@ -82,6 +82,10 @@ static_assert(sizeof(GemmParams) <= 128, "keep the kernel parameter block at 128
 constexpr int kFlagAccumulate = 0x1;  // FP32 D only: add the product onto D (D = C + A·Bᵀ, D holding C)
 constexpr int kFlagAMN = 0x2;         // dense layouts: A stored [K, M] (MN-major)
 constexpr int kFlagBMN = 0x4;         // dense layouts: B stored [K, N] (MN-major)
+// Split-K inside a thread-block cluster (dense and contiguous): one work unit per CTA, the splits
+// of a tile are the CTAs of one cluster (rank = split), and they reduce through distributed
+// shared memory instead of the global workspace.
+constexpr int kFlagClusterSplit = 0x8;
 
 struct Tile {
   int g;          // group
@@ -380,6 +384,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   using R = Roles<BN, EPI_COLS>;
   using Plan = SmemPlan<BN, STAGES, R::kEpiWarps, NBUF>;
   constexpr int kEpiWarps = R::kEpiWarps;
+  // cluster split-K (kFlagClusterSplit) is compiled into the dense and contiguous forms only
+  constexpr bool kClusterCapable = (MODE == kDense || MODE == kContiguous) && !SWIGLU;
   constexpr int kChunks = EPI_COLS / 32;   // 32-column TMEM loads per epilogue thread and K-block
   constexpr uint32_t kTmemCols = NBUF * BN;
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocation: power of two");
@@ -565,6 +571,12 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         }
       }
     }
+    if (kClusterCapable && (p.flags & kFlagClusterSplit)) {
+      // the two cluster barriers of the epilogue's reduction, which every thread must reach
+      __syncwarp();
+      cluster_sync_all();
+      cluster_sync_all();
+    }
   } else {
     // ================================================================== epilogue warpgroups
     if constexpr (R::kRebalance) setmaxnreg_inc<R::kEpiRegs>();
@@ -585,6 +597,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     float2 acc2[EPI_COLS / 2];
     float* const acc = reinterpret_cast<float*>(acc2);
 
+    bool have_partial = false;   // cluster split: this CTA's partial tile is in acc
     for (int t = blockIdx.x; alive && t < stash[11]; t += gridDim.x) {
       int kb_begin, kb_end;
       {
@@ -669,6 +682,10 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         }
       }
       if (!alive) break;
+      if (kClusterCapable && (p.flags & kFlagClusterSplit)) {   // one unit per CTA: the reduction follows the loop
+        have_partial = true;
+        break;
+      }
       // the rest of the tile description, back from shared memory
       tile.split = stash[3]; tile.out_idx = stash[4]; tile.a_row = stash[5]; tile.splits = stash[7];
 
@@ -912,6 +929,60 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           }
         }
       }
+    }
+    if constexpr (kClusterCapable) if (p.flags & kFlagClusterSplit) {
+      // Split-K in a cluster. The S CTAs of the cluster computed the S K ranges of one tile (cluster
+      // rank = split). Each writes its FP32 partial into its own stage buffers, idle once the K loop
+      // is done. After a cluster barrier, each CTA sums the partials of an interleaved set of rows
+      // (row r goes to rank r % S) in split order 0..S-1, reading its peers' shared memory, and
+      // stores those rows of D. A second barrier keeps every CTA's shared memory in place until its
+      // peers have read it. Every thread of the cluster reaches both barriers on every path.
+      constexpr uint32_t kRowBytes = (BN + 4) * 4;   // +16 bytes a row: 32 rows cover all banks
+      static_assert(128 * kRowBytes <= STAGES * Plan::kStageBytes, "partial tile exceeds the stage buffers");
+      const uint32_t part = smem_u32(smem);
+      if (have_partial) {
+#pragma unroll
+        for (int j = 0; j < EPI_COLS; j += 4)
+          st_shared_v4(part + row_in_tile * kRowBytes + (cgrp * EPI_COLS + j) * 4, __float_as_uint(acc[j]),
+                       __float_as_uint(acc[j + 1]), __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+      }
+      cluster_sync_all();
+      if (have_partial) {
+        const int S = stash[7], g = stash[0], n_blk = stash[2], a_row = stash[5], rows = stash[6];
+        const int rank = (int)cluster_ctarank();
+        constexpr int kVec = BN / 4;                       // float4 per row
+        constexpr int kRowsPerPass = R::kEpiThreads / kVec;   // 4 (BN=256) or 8 (BN=128)
+        const int c4 = threadIdx.x % kVec;
+        const int n = n_blk * BN + c4 * 4;
+        for (int r = rank + (threadIdx.x / kVec) * S; r < rows; r += kRowsPerPass * S) {
+          float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int s = 0; s < S; ++s) {
+            const float4 v = ld_cluster_v4(cluster_map(part + r * kRowBytes + c4 * 16, (uint32_t)s));
+            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+          }
+          if (n >= p.N) continue;
+          const size_t d_row = (size_t)(a_row + r);
+          if constexpr (MODE == kContiguous) {
+            const int idx = __ldg(p.m_indices + a_row + r);
+            if (idx != g) {
+              if (idx != -1 && c4 == 0) atomicOr(p.status, kStatusBadGroup);
+              continue;   // a padding row (or another group's): left untouched
+            }
+          }
+          if constexpr (OUT_F32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.D) + d_row * p.N + n);
+            if (p.flags & kFlagAccumulate) {
+              const float4 c = *dst;
+              tot.x = c.x + tot.x; tot.y = c.y + tot.y; tot.z = c.z + tot.z; tot.w = c.w + tot.w;
+            }
+            *dst = tot;
+          } else {
+            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.D) + d_row * p.N + n) =
+                make_uint2(pack_bf16x2(tot.x, tot.y), pack_bf16x2(tot.z, tot.w));
+          }
+        }
+      }
+      cluster_sync_all();
     }
     if (lane == 0) tma_store_wait_all();
     __syncwarp();

@@ -16,6 +16,7 @@ struct LaunchArgs {
   int block_n;   // 128 or 256
   bool out_f32;
   int grid;
+  int cluster;   // > 1: launch as clusters of this many CTAs (cluster split-K)
   cudaStream_t stream;
 };
 
@@ -38,6 +39,10 @@ cudaError_t launch_kgrouped(const LaunchArgs& a);
 cudaError_t launch_masked_swiglu(const LaunchArgs& a);
 // The block-scaled kernel for packed UE8M0 scales (block_n is always 256).
 cudaError_t launch_bs(const LaunchArgs& a, Mode mode);
+// How many clusters of `cluster` CTAs of the dense / contiguous instantiation for (block_n,
+// out_f32) can be resident at once (0 if the query fails).
+int cluster_capacity_dense(int block_n, bool out_f32, int cluster);
+int cluster_capacity_contiguous(int block_n, bool out_f32, int cluster);
 
 // Launches one instantiation; sets its dynamic shared-memory limit on first use per device.
 template <int BN, Mode MODE, bool OUT_F32, bool SWIGLU = false>
@@ -58,8 +63,61 @@ cudaError_t launch_instance(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
+  if (a.cluster > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
+    cfg.blockDim = dim3(R::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Plan::kDynamicBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)a.cluster;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a.tmA, a.tmB, a.tmD, a.p);
+  }
   kernel<<<a.grid, R::kThreads, Plan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
   return cudaGetLastError();
+}
+
+// Resident clusters of `cluster` CTAs for one instantiation (an occupancy query; nothing runs).
+template <int BN, Mode MODE, bool OUT_F32>
+int cluster_capacity_instance(int cluster) {
+  constexpr int STAGES = stages_for(BN);
+  constexpr int EPI_COLS = epi_cols_for(BN);
+  constexpr int NBUF = tmem_bufs_for(BN);
+  using R = Roles<BN, EPI_COLS>;
+  using Plan = SmemPlan<BN, STAGES, R::kEpiWarps, NBUF>;
+  auto kernel = fp8_gemm_kernel<BN, EPI_COLS, STAGES, NBUF, MODE, OUT_F32, false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Plan::kDynamicBytes) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+  cfg.blockDim = dim3(R::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Plan::kDynamicBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();   // clear the error: the caller falls back to the global split-K
+    return 0;
+  }
+  return n;
+}
+
+template <Mode MODE>
+int cluster_capacity_mode(int block_n, bool out_f32, int cluster) {
+  if (block_n == 256)
+    return out_f32 ? cluster_capacity_instance<256, MODE, true>(cluster) : cluster_capacity_instance<256, MODE, false>(cluster);
+  return out_f32 ? cluster_capacity_instance<128, MODE, true>(cluster) : cluster_capacity_instance<128, MODE, false>(cluster);
 }
 
 template <Mode MODE, bool OUT_F32>

@@ -102,3 +102,12 @@ def test_tail_split_setting_is_host_state():
         assert dg.dg_set_tail_splits(prev) == 4
     finally:
         dg.dg_set_tail_splits(prev)
+
+
+def test_cluster_split_setting_is_host_state():
+    prev = dg.dg_set_cluster_split(False)
+    try:
+        assert dg.dg_set_cluster_split(True) is False
+        assert dg.dg_set_cluster_split(True) is True
+    finally:
+        dg.dg_set_cluster_split(prev)
