@@ -299,7 +299,7 @@ int dg_get_num_sms(void);
    152 SMs. */
 int dg_set_tail_splits(int n);
 
-/* Split-K inside thread-block clusters (dense and contiguous forms with FP32 scales). When a call
+/* Split-K inside thread-block clusters (dense and contiguous forms, either scale form). When a call
    splits K (few output tiles) into at most 8 ranges and every tile's ranges fit on the GPU at once
    as one cluster of CTAs, the ranges reduce through distributed shared memory: partials in each
    CTA's shared memory, cluster barriers, sums in range order. Otherwise they go through a global

@@ -63,21 +63,26 @@ bool cluster_split_setting() {
 constexpr int kMaxClusterSplit = 8;
 
 // Resident clusters of `splits` CTAs for an instantiation, queried once per device.
-int cluster_capacity(int mode, int block_n, bool out_f32, int splits) {
+int cluster_capacity(int mode, int block_n, bool out_f32, int splits, bool block_scaled) {
   static std::mutex mu;
-  static int cache[kMaxDevices][2][2][2][kMaxClusterSplit + 1];
-  static bool have[kMaxDevices][2][2][2][kMaxClusterSplit + 1];
+  static int cache[kMaxDevices][2][2][2][2][kMaxClusterSplit + 1];
+  static bool have[kMaxDevices][2][2][2][2][kMaxClusterSplit + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   if (splits < 2 || splits > kMaxClusterSplit || (mode != dg::kDense && mode != dg::kContiguous)) return 0;
-  const int m = mode == dg::kDense ? 0 : 1, b = block_n == 256 ? 1 : 0, f = out_f32 ? 1 : 0;
+  const int k = block_scaled ? 1 : 0, m = mode == dg::kDense ? 0 : 1, b = block_n == 256 ? 1 : 0, f = out_f32 ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (!have[dev][m][b][f][splits]) {
-    cache[dev][m][b][f][splits] = m == 0 ? dg::cluster_capacity_dense(block_n, out_f32, splits)
-                                         : dg::cluster_capacity_contiguous(block_n, out_f32, splits);
-    have[dev][m][b][f][splits] = true;
+  if (!have[dev][k][m][b][f][splits]) {
+    int n;
+    if (block_scaled)
+      n = dg::cluster_capacity_bs(static_cast<dg::Mode>(mode), out_f32, splits);
+    else
+      n = m == 0 ? dg::cluster_capacity_dense(block_n, out_f32, splits)
+                 : dg::cluster_capacity_contiguous(block_n, out_f32, splits);
+    cache[dev][k][m][b][f][splits] = n;
+    have[dev][k][m][b][f][splits] = true;
   }
-  return cache[dev][m][b][f][splits];
+  return cache[dev][k][m][b][f][splits];
 }
 
 int tail_splits_setting() {
@@ -261,13 +266,14 @@ Config choose_config(int mode, int rows, int N, int K, int G, int num_sms, bool 
 // 64x2112x7168, 7 splits through the global workspace versus 6 in clusters. An explicit DG_SPLITS is
 // left alone.
 void fit_cluster_splits(Config& c, int mode, int K, bool block_scaled, bool out_f32) {
-  if (block_scaled || (mode != dg::kDense && mode != dg::kContiguous) || c.splits < 3) return;
+  if ((mode != dg::kDense && mode != dg::kContiguous) || c.splits < 3) return;
   if (!cluster_split_setting() || std::getenv("DG_SPLITS")) return;
-  if (c.splits <= kMaxClusterSplit && cluster_capacity(mode, c.block_n, out_f32, c.splits) >= c.tiles) return;
+  if (c.splits <= kMaxClusterSplit && cluster_capacity(mode, c.block_n, out_f32, c.splits, block_scaled) >= c.tiles)
+    return;
   const int nkb = ceil_div(K, 128);
   for (int s = c.splits - 1; s >= 2 && s >= c.splits - 2; --s) {
     const int kps = ceil_div(nkb, s), eff = ceil_div(nkb, kps);
-    if (eff >= 2 && eff <= kMaxClusterSplit && cluster_capacity(mode, c.block_n, out_f32, eff) >= c.tiles) {
+    if (eff >= 2 && eff <= kMaxClusterSplit && cluster_capacity(mode, c.block_n, out_f32, eff, block_scaled) >= c.tiles) {
       c.splits = eff;
       c.kb_per_split = kps;
       c.grid = c.tiles * eff;
@@ -276,12 +282,12 @@ void fit_cluster_splits(Config& c, int mode, int K, bool block_scaled, bool out_
   }
 }
 
-// Whether a call with this configuration runs its split-K in clusters: FP32 scales, dense or
-// contiguous, 2..8 splits, one work unit per CTA, and every tile's cluster resident at once.
+// Whether a call with this configuration runs its split-K in clusters: dense or contiguous (either
+// kernel), 2..8 splits, one work unit per CTA, and every tile's cluster resident at once.
 bool use_cluster_split(const Config& c, int mode, bool out_f32, bool block_scaled, bool swiglu) {
-  return !block_scaled && !swiglu && (mode == dg::kDense || mode == dg::kContiguous) && c.splits > 1 &&
+  return !swiglu && (mode == dg::kDense || mode == dg::kContiguous) && c.splits > 1 &&
          c.splits <= kMaxClusterSplit && cluster_split_setting() && c.grid == c.tiles * c.splits &&
-         cluster_capacity(mode, c.block_n, out_f32, c.splits) >= c.tiles;
+         cluster_capacity(mode, c.block_n, out_f32, c.splits, block_scaled) >= c.tiles;
 }
 
 // Read on every call (a debugging aid), so that a process can switch it on and off.

@@ -92,6 +92,8 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
   constexpr int EPI_COLS = 128;
   constexpr int STAGES = Plan::kStages;
   constexpr int SLOTS = Plan::kSfSlots;
+  // cluster split-K (kFlagClusterSplit) is compiled into the dense and contiguous forms only
+  constexpr bool kClusterCapable = MODE == kDense || MODE == kContiguous;
   constexpr uint32_t kIdesc = make_idesc_e4m3_bs(128, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -323,6 +325,12 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         post(end_mark, 1);
       }
     }
+    if (kClusterCapable && (p.flags & kFlagClusterSplit)) {
+      // the two cluster barriers of the epilogue's reduction, which every thread must reach
+      __syncwarp();
+      cluster_sync_all();
+      cluster_sync_all();
+    }
   } else {
     // ================================================================== epilogue warpgroups
     setmaxnreg_inc<R::kEpiRegs>();
@@ -339,6 +347,9 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
     // the 128 accumulator registers and the description are not live together.
     volatile int* stash = reinterpret_cast<volatile int*>(smem + Plan::kStashOff + warp * 64);
 
+    bool have_partial = false;   // cluster split: this CTA's partial tile is in its stage buffers
+    constexpr uint32_t kRowBytes = (BN + 4) * 4;   // partial rows in shared memory, +16 bytes: all banks
+    static_assert(128 * kRowBytes <= STAGES * Plan::kStageBytes, "partial tile exceeds the stage buffers");
     while (alive) {
       // the next tile's description, copied into this warp's stash before its slot is released
       bool active;
@@ -389,6 +400,19 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       const bool row_exists = row_in_tile < tile.rows;
       const int n_col0 = tile.n_blk * BN + cgrp * EPI_COLS;
       const bool col_exists = n_col0 < p.N;
+
+      if (kClusterCapable && (p.flags & kFlagClusterSplit)) {
+        // one unit per CTA: the partial goes to this CTA's stage buffers (idle once the MMA is
+        // done) and the reduction follows the loop. Rows or columns outside the tile (a warp that
+        // loaded nothing) are written but never read.
+        const uint32_t part = smem_u32(smem);
+#pragma unroll
+        for (int j = 0; j < EPI_COLS; j += 4)
+          st_shared_v4(part + row_in_tile * kRowBytes + (cgrp * EPI_COLS + j) * 4, accu[j], accu[j + 1], accu[j + 2],
+                       accu[j + 3]);
+        have_partial = true;
+        break;
+      }
 
       // ---------------- split-K: publish the partial, and let the last split reduce
       if (tile.splits > 1) {
@@ -523,6 +547,51 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
           }
         }
       }
+    }
+    if constexpr (kClusterCapable) if (p.flags & kFlagClusterSplit) {
+      // Split-K in a cluster, as in the FP32-scale kernel: the S CTAs of the cluster hold the S K
+      // ranges of one tile (rank = range); after a cluster barrier each sums the rows r with
+      // r % S = rank in range order from its peers' shared memory and stores them; a second barrier
+      // keeps every CTA's shared memory in place until its peers have read it. Every thread of the
+      // cluster reaches both barriers on every path.
+      const uint32_t part = smem_u32(smem);
+      cluster_sync_all();
+      if (have_partial) {
+        const int S = stash[3] >> 16, g = stash[0], n_blk = stash[2], a_row = stash[5], rows = stash[6];
+        const int rank = (int)cluster_ctarank();
+        constexpr int kVec = BN / 4;                       // float4 per row
+        constexpr int kRowsPerPass = R::kEpiThreads / kVec;
+        const int c4 = threadIdx.x % kVec;
+        const int n = n_blk * BN + c4 * 4;
+        for (int r = rank + (threadIdx.x / kVec) * S; r < rows; r += kRowsPerPass * S) {
+          float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int s = 0; s < S; ++s) {
+            const float4 v = ld_cluster_v4(cluster_map(part + r * kRowBytes + c4 * 16, (uint32_t)s));
+            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+          }
+          if (n >= p.N) continue;
+          const size_t d_row = (size_t)(a_row + r);
+          if constexpr (MODE == kContiguous) {
+            const int idx = __ldg(p.m_indices + a_row + r);
+            if (idx != g) {
+              if (idx != -1 && c4 == 0) atomicOr(p.status, kStatusBadGroup);
+              continue;   // a padding row (or another group's): left untouched
+            }
+          }
+          if constexpr (OUT_F32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.D) + d_row * p.N + n);
+            if (p.flags & kFlagAccumulate) {
+              const float4 c = *dst;
+              tot.x = c.x + tot.x; tot.y = c.y + tot.y; tot.z = c.z + tot.z; tot.w = c.w + tot.w;
+            }
+            *dst = tot;
+          } else {
+            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.D) + d_row * p.N + n) =
+                make_uint2(pack_bf16x2(tot.x, tot.y), pack_bf16x2(tot.z, tot.w));
+          }
+        }
+      }
+      cluster_sync_all();
     }
     if (lane == 0) tma_store_wait_all();
     __syncwarp();

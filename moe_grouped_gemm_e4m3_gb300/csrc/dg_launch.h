@@ -43,6 +43,52 @@ cudaError_t launch_bs(const LaunchArgs& a, Mode mode);
 // out_f32) can be resident at once (0 if the query fails).
 int cluster_capacity_dense(int block_n, bool out_f32, int cluster);
 int cluster_capacity_contiguous(int block_n, bool out_f32, int cluster);
+// The same for the block-scaled kernel (dense or contiguous).
+int cluster_capacity_bs(Mode mode, bool out_f32, int cluster);
+
+// Launches `kernel` as clusters of `cluster` CTAs (1-D grid of `grid` CTAs).
+template <typename Kernel>
+cudaError_t launch_clustered(Kernel kernel, const LaunchArgs& a, int threads, size_t smem_bytes) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)a.cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a.tmA, a.tmB, a.tmD, a.p);
+}
+
+// Resident clusters of `cluster` CTAs of `kernel` (an occupancy query; nothing runs; 0 on error).
+template <typename Kernel>
+int clusters_resident(Kernel kernel, int threads, size_t smem_bytes, int cluster) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();   // clear the error: the caller falls back to the global split-K
+    return 0;
+  }
+  return n;
+}
 
 // Launches one instantiation; sets its dynamic shared-memory limit on first use per device.
 template <int BN, Mode MODE, bool OUT_F32, bool SWIGLU = false>
@@ -63,21 +109,7 @@ cudaError_t launch_instance(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  if (a.cluster > 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
-    cfg.blockDim = dim3(R::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Plan::kDynamicBytes;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = (unsigned)a.cluster;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a.tmA, a.tmB, a.tmD, a.p);
-  }
+  if (a.cluster > 1) return launch_clustered(kernel, a, R::kThreads, Plan::kDynamicBytes);
   kernel<<<a.grid, R::kThreads, Plan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
   return cudaGetLastError();
 }
@@ -90,27 +122,8 @@ int cluster_capacity_instance(int cluster) {
   constexpr int NBUF = tmem_bufs_for(BN);
   using R = Roles<BN, EPI_COLS>;
   using Plan = SmemPlan<BN, STAGES, R::kEpiWarps, NBUF>;
-  auto kernel = fp8_gemm_kernel<BN, EPI_COLS, STAGES, NBUF, MODE, OUT_F32, false>;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Plan::kDynamicBytes) !=
-      cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
-  cfg.blockDim = dim3(R::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Plan::kDynamicBytes;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = (unsigned)cluster;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
-    cudaGetLastError();   // clear the error: the caller falls back to the global split-K
-    return 0;
-  }
-  return n;
+  return clusters_resident(fp8_gemm_kernel<BN, EPI_COLS, STAGES, NBUF, MODE, OUT_F32, false>, R::kThreads,
+                           Plan::kDynamicBytes, cluster);
 }
 
 template <Mode MODE>
@@ -133,6 +146,7 @@ cudaError_t launch_bs_instance(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
+  if (a.cluster > 1) return launch_clustered(kernel, a, BsRoles::kThreads, BsSmemPlan::kDynamicBytes);
   kernel<<<a.grid, BsRoles::kThreads, BsSmemPlan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
   return cudaGetLastError();
 }

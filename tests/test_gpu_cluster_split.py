@@ -136,3 +136,71 @@ def test_cluster_split_accumulate_and_layout(dg, capfd):
     assert np.array_equal(dnn.view(np.int32), d32.view(np.int32)), "NN layout differs from NT"
     for x, y in ((d32, d32_off), (acc, acc_off), (dnn, dnn_off)):
         assert np.array_equal(x.view(np.int32), y.view(np.int32))
+
+
+def _ue8m0(a, b):
+    """Packed UE8M0 words (what the GPU gets) and the FP32 scales the oracle decodes from them."""
+    nkb = -(-a.A.shape[-1] // 128)
+    pa, pb = dg_inputs.pack_ue8m0_a(a.sA), dg_inputs.pack_ue8m0_b(b.sB)
+    return pa, pb, oracle.unpack_ue8m0_a(pa, nkb), oracle.unpack_ue8m0_b(pb, nkb)
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 7168, 16384), (64, 4096, 7168), (64, 2112, 7168), (128, 512, 1024)])
+def test_cluster_split_dense_ue8m0(dg, capfd, M, N, K):
+    cfg = dg.dg_query_config_ue8m0(0, M, N, K)
+    if not (2 <= cfg["splits"] <= 8):
+        pytest.skip(f"configuration does not split K into 2..8 ranges: {cfg}")
+    a = dg_inputs.make_a(M, K, seed=M + N + 1, ue8m0=True)
+    b = dg_inputs.make_b(1, N, K, seed=M + N + 1, ue8m0=True)
+    pa, pb, osA, osB = _ue8m0(a, b)
+    A, sA, B, sB = dev(a.A), dev(pa), dev(b.B[0]), dev(pb[0])
+
+    def run():
+        D = bf16_sentinel((M, N))
+        D32 = f32_sentinel((M, N))
+        dg.dg_fp8_gemm_nt_ue8m0(A, sA, B, sB, D)
+        dg.dg_fp8_gemm_nt_ue8m0_f32(A, sA, B, sB, D32)
+        torch.cuda.synchronize()
+        return bits16(D).cpu(), D32.cpu()
+
+    (d_on, f_on), (d_off, f_off) = _both(dg, run, capfd)
+    prev = dg.dg_set_cluster_split(False)
+    try:
+        cfg_off = dg.dg_query_config_ue8m0(0, M, N, K)
+    finally:
+        dg.dg_set_cluster_split(prev)
+    if cfg_off["splits"] == cfg["splits"]:
+        assert torch.equal(d_on, d_off) and torch.equal(f_on.view(torch.int32), f_off.view(torch.int32))
+    assert torch.equal(d_on, rne_bf16_bits(f_on))
+    ms, ns = boundary_samples(M, N, 1500, seed=4, block_cols=128)
+    ref = oracle.gemm_nt_sampled(a.A, osA, b.B[0], osB[0], ms, ns)
+    assert_accurate(f_on.numpy()[ms, ns], d_on.numpy()[ms, ns], ref, f"ue8m0 cluster split {M}x{N}x{K}")
+    assert_accurate(f_off.numpy()[ms, ns], d_off.numpy()[ms, ns], ref, f"ue8m0 global split {M}x{N}x{K}")
+
+
+def test_cluster_split_contiguous_ue8m0_with_padding(dg, capfd):
+    m_idx = dg_inputs.contiguous_m_indices([70, 0, 120])
+    rows, N, K, G = len(m_idx), 1024, 4096, 3
+    cfg = dg.dg_query_config_ue8m0(1, rows, N, K, G)
+    if not (2 <= cfg["splits"] <= 8):
+        pytest.skip(f"configuration does not split K into 2..8 ranges: {cfg}")
+    a = dg_inputs.make_a(rows, K, seed=10, ue8m0=True)
+    b = dg_inputs.make_b(G, N, K, seed=10, ue8m0=True)
+    pa, pb, osA, osB = _ue8m0(a, b)
+    A, sA, B, sB, I = dev(a.A), dev(pa), dev(b.B), dev(pb), dev(m_idx)
+
+    def run():
+        D32 = f32_sentinel((rows, N))
+        dg.dg_fp8_grouped_contiguous_ue8m0_f32(A, sA, B, sB, I, D32)
+        torch.cuda.synchronize()
+        return D32.cpu()
+
+    f_on, f_off = _both(dg, run, capfd)
+    pad = torch.from_numpy(m_idx < 0)
+    assert bool(torch.isnan(f_on[pad]).all()), "padding rows were written"
+    v = m_idx >= 0
+    ref64, _, _ = oracle.grouped_contiguous(a.A, osA, b.B, osB, m_idx)
+    for f, what in ((f_on, "on"), (f_off, "off")):
+        d = f.numpy()[v]
+        bits = torch.from_numpy(d.copy()).to(torch.bfloat16).view(torch.int16).numpy()
+        assert_accurate(d, bits, ref64[v], f"ue8m0 cluster split contiguous {what}")
