@@ -160,6 +160,18 @@ def measured_traffic(shape: str):
     return int(launch["dram_read_bytes"] + launch["dram_write_bytes"])
 
 
+def slowest_rank(value: float, pg) -> float:
+    """The largest `value` over all ranks, returned on every rank (the job's time is its slowest
+    rank's); `value` itself without a process group. NCCL reduces on the GPU, gloo on the host."""
+    if pg is None:
+        return value
+    import torch
+    device = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    x = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(x, op=pg.ReduceOp.MAX)
+    return float(x.item())
+
+
 def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -331,11 +343,7 @@ def run_ours(args, rank, world, local):
     per_shape_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(len(tensors))]
                              for s in range(args.steps)])   # [steps, shapes]
     ms_per_step_local = float(per_shape_ms.sum(axis=1).mean())
-    ms_per_step = ms_per_step_local
-    if pg:
-        x = torch.tensor([ms_per_step_local], dtype=torch.float64, device="cuda")
-        pg.all_reduce(x, op=pg.ReduceOp.MAX)
-        ms_per_step = float(x.item())
+    ms_per_step = slowest_rank(ms_per_step_local, pg)
     status = dg.dg_get_device_status()
     if status:
         raise RuntimeError(f"device status 0x{status:x} after the timed region")
@@ -348,9 +356,7 @@ def run_ours(args, rank, world, local):
     if not args.no_e2e:
         e2e = measure_e2e(dg, problems, args, stream)
         if pg:
-            x = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
-            pg.all_reduce(x, op=pg.ReduceOp.MAX)
-            e2e["value"] = world * flops_step / (float(x.item()) * 1e-3) / 1e12
+            e2e["value"] = world * flops_step / (slowest_rank(e2e["ms_per_step"], pg) * 1e-3) / 1e12
 
     if rank != 0:
         if pg:
