@@ -38,10 +38,14 @@
  *   pipeline wait that timed out) never trap: the kernel skips the affected rows or tiles, sets
  *   bits of a device status word and returns. Read it with dg_get_device_status().
  * - Split-K: for small problems the library may split K across CTAs and reduce the FP32
- *   partials in a fixed order (deterministic). Its workspace is a library-owned buffer per
- *   device, allocated on the first call that needs it and grown when a larger one is needed
- *   (that call allocates; make it before any CUDA-graph capture). Calls that use the workspace
- *   and overlap on the GPU (different streams of one device) race on it.
+ *   partials in a fixed order (deterministic). Where the ranges of every tile fit on the GPU at
+ *   once as thread-block clusters, they reduce through distributed shared memory and use no
+ *   workspace (dg_set_cluster_split). Otherwise, and for the tail split (dg_set_tail_splits), the
+ *   partials go to a library-owned buffer per device. It is allocated on the first call that needs
+ *   it and grown when a larger one is needed; that call allocates, so make it before any CUDA-graph
+ *   capture. Calls that use the workspace and overlap on the GPU (different streams of one device)
+ *   race on it. The first call that considers clusters for a kernel also queries, once per device,
+ *   how many of its clusters fit (cudaOccupancyMaxActiveClusters; no launch, no allocation).
  */
 #ifndef DG_H
 #define DG_H
