@@ -15,10 +15,12 @@
 // register accumulators, FFMA yield-bit interleaving — is prior art, not the blueprint):
 //   * producer warp: TMA loads of 128x128-byte A tiles and BNx128-byte B tiles (128-byte swizzle)
 //     into a STAGES-deep shared-memory ring guarded by full/empty mbarriers;
-//   * MMA warp: one elected thread issues 4 tcgen05.mma.kind::f8f6f4 (K = 32 each) per 128-deep
-//     K-block into one of two TMEM accumulators (128 lanes x BN FP32 columns each), a fresh
-//     accumulator per K-block, then tcgen05.commit frees the smem stage and publishes the TMEM
-//     buffer;
+//   * two MMA warps: one thread of each issues 4 tcgen05.mma.kind::f8f6f4 (K = 32 each) per
+//     128-deep K-block, alternating K-blocks, into a ring of TMEM accumulators (128 lanes x BN FP32
+//     columns each), a fresh accumulator per K-block; tcgen05.commit then frees the smem stage and
+//     publishes the TMEM buffer. (Each tcgen05 instruction holds its issuing thread for about 50
+//     cycles: one thread alone cannot issue a K-block's waits, MMAs and commits in the 512 cycles
+//     the tensor core takes to run it.)
 //   * epilogue warps (BN/32 of them; warp w owns TMEM lanes 32*(w%4).. and 128 columns
 //     starting at 128*(w/4)): tcgen05.ld the K-block's partial, scale it by sA·sB and add it into
 //     128 FP32 registers per thread with packed fma.rn.f32x2; release the TMEM buffer right after
@@ -290,8 +292,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Sched& sc
 // Warp roles, register split and shared-memory plan.
 //
 // Epilogue warps come first, 4 per EPI_COLS-wide column group (one per 32-lane TMEM quadrant);
-// then one more warpgroup holds the producer warp, the MMA warp and two idle warps, so that every
-// warpgroup is whole and can rebalance registers with setmaxnreg.
+// then one more warpgroup holds the producer warp, the two MMA-issuing warps and an idle warp, so
+// that every warpgroup is whole and can rebalance registers with setmaxnreg.
 
 template <int BN, int EPI_COLS>
 struct Roles {
@@ -301,7 +303,8 @@ struct Roles {
   static constexpr int kEpiWarps = 4 * (BN / EPI_COLS);
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kProducerWarp = kEpiWarps;
-  static constexpr int kMmaWarp = kEpiWarps + 1;
+  static constexpr int kMmaWarp = kEpiWarps + 1;    // allocates TMEM; issues the even K-blocks
+  static constexpr int kMmaWarp2 = kEpiWarps + 2;   // issues the odd K-blocks
   static constexpr int kWarps = kEpiWarps + 4;
   static constexpr int kThreads = kWarps * 32;
   // Registers per thread at launch (65536 per SM, allocated for whole 4-warp groups).
@@ -519,36 +522,49 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           }
         }
       }
-    } else if (warp == R::kMmaWarp) {
-      // ---------------------------------------------------------------- tcgen05 MMA issuer
-      uint32_t it = 0, acc_it = 0;
+    } else if (warp == R::kMmaWarp || warp == R::kMmaWarp2) {
+      // ---------------------------------------------------------------- tcgen05 MMA issuers
+      // Two threads issue the MMAs: issuer `me` takes the K-blocks whose running index (over all
+      // of this CTA's tiles) is congruent to `me` mod 2, so each has two K-blocks of tensor time for
+      // its two waits, four MMAs and two commits. Issuing one tcgen05 instruction blocks the issuing
+      // thread for about 50 cycles, so one thread alone needs more time per K-block (waits,
+      // 4 MMAs, 2 commits) than the tensor core takes to run it. K-blocks use separate TMEM
+      // buffers and stages, so the order in which the two threads issue them does not matter;
+      // each commit covers only its own thread's MMAs.
+      const uint32_t me = (uint32_t)(warp - R::kMmaWarp);
+      const bool a_mn = (p.flags & kFlagAMN) != 0, b_mn = (p.flags & kFlagBMN) != 0;
+      const uint32_t a_addr0 = smem_u32(smem);
+      const uint64_t adesc0 = a_mn ? make_sw128_mnmajor_desc(a_addr0, 128 * 128) : make_sw128_kmajor_desc(a_addr0);
+      const uint64_t bdesc0 = b_mn ? make_sw128_mnmajor_desc(a_addr0 + Plan::kABytes, 128 * 128)
+                                   : make_sw128_kmajor_desc(a_addr0 + Plan::kABytes);
+      // one K=32 step: +32 bytes inside a K-major 128-byte row (+2 in the >>4 address field), or
+      // +32 rows of 128 bytes in an MN-major tile (+256)
+      const uint32_t a_step = a_mn ? 256u : 2u, b_step = b_mn ? 256u : 2u;
+      const uint32_t idesc = kIdesc | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
+      uint32_t acc_it = 0;   // running K-block index of the CTA (both issuers count every K-block)
       bool alive = true;
       int last_b = -1;
       uint32_t last_ph = 0;
       for (int t = blockIdx.x; alive && t < total_units; t += gridDim.x) {
         const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
-        // Lane 0 runs the tile's K loop on its own (no warp-wide step per K-block).
+        const uint32_t nk = (uint32_t)(tile.kb1 - tile.kb0);
+        // Lane 0 runs this issuer's K-blocks of the tile on its own (no warp-wide step per K-block).
         int ok = 1;
         if (lane == 0) {
-          for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it, ++acc_it) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1;
-            const int b = acc_it % NBUF;
-            const uint32_t aph = (acc_it / NBUF) & 1;
-            ok = mbar_wait(&tempty_bar[b], aph ^ 1, abort_flag, p.status) &&
-                 mbar_wait(&full_bar[s], ph, abort_flag, p.status);
+          for (uint32_t g = acc_it + ((me - acc_it) & 1u); g < acc_it + nk; g += 2) {
+            const int s = (int)(g % STAGES);
+            const uint32_t ph = (g / STAGES) & 1;
+            const int b = (int)(g % NBUF);
+            const uint32_t aph = (g / NBUF) & 1;
+            // the stage's data first (normally there long before), then the TMEM buffer, whose
+            // release by the epilogue is the round trip this wait is on
+            ok = mbar_wait(&full_bar[s], ph, abort_flag, p.status) &&
+                 mbar_wait(&tempty_bar[b], aph ^ 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
-            const bool a_mn = (p.flags & kFlagAMN) != 0, b_mn = (p.flags & kFlagBMN) != 0;
-            const uint64_t adesc = a_mn ? make_sw128_mnmajor_desc(a_addr, 128 * 128) : make_sw128_kmajor_desc(a_addr);
-            const uint64_t bdesc = b_mn ? make_sw128_mnmajor_desc(a_addr + Plan::kABytes, 128 * 128)
-                                        : make_sw128_kmajor_desc(a_addr + Plan::kABytes);
-            // one K=32 step: +32 bytes inside a K-major 128-byte row (+2 in the >>4 address field), or
-            // +32 rows of 128 bytes in an MN-major tile (+256)
-            const uint32_t a_step = a_mn ? 256u : 2u, b_step = b_mn ? 256u : 2u;
-            const uint32_t idesc = kIdesc | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
+            const uint64_t soff = (uint64_t)((s * Plan::kStageBytes) >> 4);
+            const uint64_t adesc = adesc0 + soff, bdesc = bdesc0 + soff;
             const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -560,11 +576,12 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             last_ph = aph;
           }
         }
+        acc_it += nk;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) { alive = false; break; }
       }
       if (!alive && lane == 0 && last_b >= 0) {
-        // Abandoned: wait for the MMAs already issued before TMEM is freed.
+        // Abandoned: wait for the MMAs this thread issued before TMEM is freed.
         const uint32_t a = smem_u32(&tfull_bar[last_b]);
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(a, last_ph) && global_timer_ns() - t0 < kWaitLimitNs) {
@@ -612,36 +629,41 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         kb_end = tile0.kb1;
       }
       __syncwarp();
-      Tile tile;
-      tile.g = stash[0]; tile.m_blk = stash[1]; tile.n_blk = stash[2];
-      tile.rows = stash[6];
-      const int m_local = tile.m_blk * 128 + row_in_tile;   // row within the group
-      const bool row_exists = row_in_tile < tile.rows;
-      const float* sa_ptr = p.sA + (MODE == kMasked ? (size_t)tile.g * p.nkb * p.ldsa : 0) + m_local;
-      // first column of this warp (as a row of B: fused SwiGLU puts the up rows at I + 128·n)
-      const int n_col0 = SWIGLU ? (cgrp ? p.swiglu_i : 0) + tile.n_blk * 128 : tile.n_blk * BN + cgrp * EPI_COLS;
-      const bool col_exists = n_col0 < p.N;
-      const float* sb_ptr = p.sB + ((size_t)(MODE == kKGrouped ? 0 : tile.g) * p.nnb + (col_exists ? n_col0 / 128 : 0)) * p.nkb;
-      // Warps with no row or no column in range only keep the TMEM handshake going.
-      const bool active = col_exists && __any_sync(0xffffffffu, row_exists);
+      // The first column of this warp (as a row of B: fused SwiGLU puts the up rows at I + 128·n).
+      auto first_col = [&](int n_blk) -> int {
+        return SWIGLU ? (cgrp ? p.swiglu_i : 0) + n_blk * 128 : n_blk * BN + cgrp * EPI_COLS;
+      };
+      // Only what the K loop needs is live across it; the rest of the tile is re-read afterwards.
+      const float* sa_ptr;
+      const float* sb_ptr;
+      bool active, row_live;
+      {
+        const int g = stash[0], n_col = first_col(stash[2]);
+        row_live = row_in_tile < stash[6];
+        const bool col_live = n_col < p.N;
+        sa_ptr = p.sA + (MODE == kMasked ? (size_t)g * p.nkb * p.ldsa : 0) + stash[1] * 128 + row_in_tile;
+        sb_ptr = p.sB + ((size_t)(MODE == kKGrouped ? 0 : g) * p.nnb + (col_live ? n_col / 128 : 0)) * p.nkb;
+        // Warps with no row or no column in range only keep the TMEM handshake going.
+        active = col_live && __any_sync(0xffffffffu, row_live);
+      }
 
 #pragma unroll
       for (int i = 0; i < EPI_COLS; ++i) acc[i] = 0.0f;
 
-      // scales of the first K-block; later ones are fetched one K-block ahead
-      // (a K-grouped tile can have an empty K range: it stores zeros and reads no scale)
-      const bool any_kb = kb_begin < kb_end;
-      float sa_next = (active && row_exists && any_kb) ? __ldg(sa_ptr + (size_t)kb_begin * p.ldsa) : 0.0f;
-      float sb_next = (active && any_kb) ? __ldg(sb_ptr + kb_begin) : 0.0f;
+      // Scales: K-block kb uses sA[m,kb]·sB[nb,kb]. The pair for kb + 1 is requested at the top of
+      // step kb, before its wait, and moved into place at the end of it, so a global load has the
+      // step's wait, TMEM loads and FMAs to land. (A K-grouped tile can have an empty K range: it
+      // stores zeros and reads no scale.)
+      auto fetch_sa = [&](int kb) -> float {
+        return (active && row_live && kb < kb_end) ? __ldg(sa_ptr + (size_t)kb * p.ldsa) : 0.0f;
+      };
+      auto fetch_sb = [&](int kb) -> float { return (active && kb < kb_end) ? __ldg(sb_ptr + kb) : 0.0f; };
+      float sa_cur = fetch_sa(kb_begin), sb_cur = fetch_sb(kb_begin);
 
       for (int kb = kb_begin; kb < kb_end; ++kb, ++acc_it) {
         const int b = acc_it % NBUF;
         const uint32_t aph = (acc_it / NBUF) & 1;
-        const float scale = sa_next * sb_next;
-        if (active && kb + 1 < kb_end) {
-          sa_next = row_exists ? __ldg(sa_ptr + (size_t)(kb + 1) * p.ldsa) : 0.0f;
-          sb_next = __ldg(sb_ptr + kb + 1);
-        }
+        const float sa_nxt = fetch_sa(kb + 1), sb_nxt = fetch_sb(kb + 1);
         // All 32 lanes wait together: one warp-wide instruction stream, uniform by construction
         // (every lane sees the same barrier phase, timer value and abort flag).
         if (!mbar_wait(&tfull_bar[b], aph, abort_flag, p.status)) { alive = false; break; }
@@ -649,6 +671,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         if (active) {
           const uint32_t taddr =
               tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN + cgrp * EPI_COLS);
+          float2 scale2 = make_float2(0.0f, 0.0f);
           // two 32-column loads in flight per wait; the buffer is released as soon as the last
           // pair has landed in registers, before its FMAs
 #pragma unroll
@@ -663,7 +686,10 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&tempty_bar[b]);
             }
-            const float2 scale2 = make_float2(scale, scale);
+            if (c == 0) {
+              const float scale = sa_cur * sb_cur;
+              scale2 = make_float2(scale, scale);
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               acc2[c * 16 + j] = __ffma2_rn(make_float2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1])),
@@ -680,14 +706,22 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty_bar[b]);
         }
+        sa_cur = sa_nxt;
+        sb_cur = sb_nxt;
       }
       if (!alive) break;
       if (kClusterCapable && (p.flags & kFlagClusterSplit)) {   // one unit per CTA: the reduction follows the loop
         have_partial = true;
         break;
       }
-      // the rest of the tile description, back from shared memory
+      // the tile description, back from shared memory
+      Tile tile;
+      tile.g = stash[0]; tile.m_blk = stash[1]; tile.n_blk = stash[2]; tile.rows = stash[6];
       tile.split = stash[3]; tile.out_idx = stash[4]; tile.a_row = stash[5]; tile.splits = stash[7];
+      const int m_local = tile.m_blk * 128 + row_in_tile;   // row within the group
+      const bool row_exists = row_in_tile < tile.rows;
+      const int n_col0 = first_col(tile.n_blk);
+      const bool col_exists = n_col0 < p.N;
 
       // ---------------- split-K: publish the partial, and let the last split reduce
       if (tile.splits > 1) {
