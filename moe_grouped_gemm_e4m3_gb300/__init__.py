@@ -148,6 +148,36 @@ def _ptr(t, name, dtypes):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _shape(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    return tuple(int(x) for x in t.shape)
+
+
+def _expect(t, name, shape):
+    """Raises ValueError unless tensor `t` has exactly `shape` (checked before any pointer is taken,
+    so that a mis-shaped call never reaches a kernel, whose TMA boxes would read out of bounds)."""
+    got = _shape(t, name)
+    if got != tuple(shape):
+        raise ValueError(f"{name} has shape {list(got)}, expected {list(shape)}")
+
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def _align4(x):
+    return -(-x // 4) * 4
+
+
+def _scale_k(name, K):
+    """Scale entries along K: one per 128-deep K-block (FP32 scales), or one int32 word per four
+    K-blocks (packed UE8M0)."""
+    nkb = _cdiv(K, 128)
+    return _cdiv(nkb, 4) if "_ue8m0" in name else nkb
+
+
 def _fp8_types():
     import torch
     return (torch.uint8, torch.float8_e4m3fn)
@@ -168,10 +198,34 @@ def _d_types(f32: bool):
     return (torch.float32,) if f32 else (torch.bfloat16, torch.int16, torch.uint16)
 
 
+def _dense_shapes(name, A, B):
+    """(M, N, K) of a dense call: A [M, K], B [N, K] (or [1, N, K])."""
+    a, b = _shape(A, "A"), _shape(B, "B")
+    if len(a) != 2:
+        raise ValueError(f"A must be [M, K], got {list(a)}")
+    if not (len(b) == 2 or (len(b) == 3 and b[0] == 1)):
+        raise ValueError(f"B must be [N, K] (or [1, N, K]), got {list(b)}")
+    M, K = a
+    N = b[-2]
+    if b[-1] != K:
+        raise ValueError(f"B has K = {b[-1]}, A has K = {K}")
+    return M, N, K
+
+
+def _check_scales_2d(name, sA, sB, M, N, K):
+    nks = _scale_k(name, K)
+    _expect(sA, "sA", (nks, _align4(M)))
+    sb = _shape(sB, "sB")
+    want = (_cdiv(N, 128), nks)
+    if sb != want and sb != (1,) + want:
+        raise ValueError(f"sB has shape {list(sb)}, expected {list(want)}")
+
+
 def _dense(name, f32, A, sA, B, sB, D, stream):
+    M, N, K = _dense_shapes(name, A, B)
+    _check_scales_2d(name, sA, sB, M, N, K)
+    _expect(D, "D", (M, N))
     lib = load()
-    M, K = A.shape
-    N = B.shape[-2]
     _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _scale_types(name)), _ptr(B, "B", _fp8_types()),
                               _ptr(sB, "sB", _scale_types(name)), _ptr(D, "D", _d_types(f32)), M, N, K, _stream(stream)))
     return D
@@ -199,9 +253,19 @@ def dg_fp8_gemm_nt_noalloc(A, sA, B, sB, D, stream=None):
 
 def _contig(name, f32, A, sA, B, sB, m_indices, D, stream):
     import torch
+    a, b = _shape(A, "A"), _shape(B, "B")
+    if len(a) != 2 or len(b) != 3:
+        raise ValueError(f"contiguous layout: A must be [M_total, K] and B [G, N, K], got {list(a)} and {list(b)}")
+    M, K = a
+    G, N = b[0], b[1]
+    if b[2] != K:
+        raise ValueError(f"B has K = {b[2]}, A has K = {K}")
+    nks = _scale_k(name, K)
+    _expect(sA, "sA", (nks, _align4(M)))
+    _expect(sB, "sB", (G, _cdiv(N, 128), nks))
+    _expect(m_indices, "m_indices", (M,))
+    _expect(D, "D", (M, N))
     lib = load()
-    M, K = A.shape
-    G, N = B.shape[0], B.shape[1]
     _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _scale_types(name)), _ptr(B, "B", _fp8_types()),
                               _ptr(sB, "sB", _scale_types(name)), _ptr(m_indices, "m_indices", (torch.int32,)),
                               _ptr(D, "D", _d_types(f32)), M, N, K, G, _stream(stream)))
@@ -219,9 +283,20 @@ def dg_fp8_grouped_contiguous_f32(A, sA, B, sB, m_indices, D, stream=None):
 
 def _masked(name, f32, A, sA, B, sB, masked_m, D, stream):
     import torch
+    a, b = _shape(A, "A"), _shape(B, "B")
+    if len(a) != 3 or len(b) != 3:
+        raise ValueError(f"masked layout: A must be [G, M_max, K] and B [G, N, K], got {list(a)} and {list(b)}")
+    G, M_max, K = a
+    N = b[1]
+    if b[0] != G or b[2] != K:
+        raise ValueError(f"B has shape {list(b)}, expected [{G}, N, {K}]")
+    nks = _scale_k(name, K)
+    _expect(sA, "sA", (G, nks, _align4(M_max)))
+    _expect(sB, "sB", (G, _cdiv(N, 128), nks))
+    _expect(masked_m, "masked_m", (G,))
+    # the fused SwiGLU writes H = silu(gate)·up, half as wide as B's 2I rows
+    _expect(D, "H" if "swiglu" in name else "D", (G, M_max, N // 2 if "swiglu" in name else N))
     lib = load()
-    G, M_max, K = A.shape
-    N = B.shape[1]
     _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _scale_types(name)), _ptr(B, "B", _fp8_types()),
                               _ptr(sB, "sB", _scale_types(name)), _ptr(masked_m, "masked_m", (torch.int32,)),
                               _ptr(D, "D", _d_types(f32)), G, M_max, N, K, _stream(stream)))
@@ -238,9 +313,11 @@ def dg_fp8_grouped_masked_f32(A, sA, B, sB, masked_m, D, stream=None):
 
 
 def _dense_acc(name, A, sA, B, sB, C, D, stream):
+    M, N, K = _dense_shapes(name, A, B)
+    _check_scales_2d(name, sA, sB, M, N, K)
+    _expect(C, "C", (M, N))
+    _expect(D, "D", (M, N))
     lib = load()
-    M, K = A.shape
-    N = B.shape[-2]
     _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _scale_types(name)),
                               _ptr(B, "B", _fp8_types()), _ptr(sB, "sB", _scale_types(name)), _ptr(C, "C", _f32()),
                               _ptr(D, "D", _f32()), M, N, K, _stream(stream)))
@@ -257,7 +334,19 @@ def dg_fp8_gemm_nt_ue8m0_acc_f32(A, sA, B, sB, C, D, stream=None):
     return _dense_acc("dg_fp8_gemm_nt_ue8m0_acc_f32", A, sA, B, sB, C, D, stream)
 
 
+# The layouts' names: the first letter says how A is stored (n: [M, K], t: [K, M]), the second how
+# B is stored (t: [N, K], n: [K, N]).
+_LAYOUTS = {"nn": (False, True), "tn": (True, True), "tt": (True, False)}
+
+
 def _dense_layout(name, f32, A, sA, B, sB, D, M, N, K, stream):
+    a_t, b_n = _LAYOUTS[name[len("dg_fp8_gemm_"):len("dg_fp8_gemm_") + 2]]
+    M, N, K = int(M), int(N), int(K)
+    _expect(A, "A", (K, M) if a_t else (M, K))
+    _expect(B, "B", (K, N) if b_n else (N, K))
+    _expect(sA, "sA", (_cdiv(K, 128), _align4(M)))
+    _expect(sB, "sB", (_cdiv(N, 128), _cdiv(K, 128)))
+    _expect(D, "D", (M, N))
     lib = load()
     _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
                               _ptr(sB, "sB", _f32()), _ptr(D, "D", _d_types(f32)), M, N, K, _stream(stream)))
@@ -293,10 +382,19 @@ def dg_fp8_gemm_tt_f32(A, sA, B, sB, D, M, N, K, stream=None):
 
 def _k_grouped(name, f32, A, sA, B, sB, k_offsets, D, stream):
     import torch
+    a, b, o = _shape(A, "A"), _shape(B, "B"), _shape(k_offsets, "k_offsets")
+    if len(a) != 2 or len(b) != 2 or len(o) != 1 or o[0] < 1:
+        raise ValueError(f"K-grouped: A must be [K_total, M], B [K_total, N], k_offsets [G + 1]; got "
+                         f"{list(a)}, {list(b)}, {list(o)}")
+    K_total, M = a
+    N = b[1]
+    G = o[0] - 1
+    if b[0] != K_total:
+        raise ValueError(f"B has K_total = {b[0]}, A has K_total = {K_total}")
+    _expect(sA, "sA", (_cdiv(K_total, 128), _align4(M)))
+    _expect(sB, "sB", (_cdiv(N, 128), _cdiv(K_total, 128)))
+    _expect(D, "D", (G, M, N))
     lib = load()
-    K_total, M = A.shape
-    N = B.shape[1]
-    G = k_offsets.shape[0] - 1
     _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
                               _ptr(sB, "sB", _f32()), _ptr(k_offsets, "k_offsets", (torch.int32,)),
                               _ptr(D, "D", _d_types(f32)), G, M, N, K_total, _stream(stream)))
