@@ -252,7 +252,8 @@ dg_status dg_fp8_gemm_nt_ue8m0_acc_f32(const uint8_t* A, const int32_t* sA, cons
 
 /*
  * Allocation-free dense GEMM: the same computation, arguments and result as dg_fp8_gemm_nt (the
- * same kernel, tile configuration, schedule and accumulation order), for callers that cannot let a library
+ * same validation, kernel, tile configuration, schedule and accumulation order: both entry points
+ * run one code path, which differs only in where split-K scratch comes from), for callers that cannot let a library
  * call cudaMalloc — for example a framework whose caching allocator already owns the device memory,
  * or a serving loop that must not block on the device synchronisation cudaMalloc/cudaFree may do.
  * The DeepGEMM pages have no counterpart to this call; it is an addition of this library.
@@ -287,9 +288,22 @@ int dg_get_mk_alignment_for_contiguous_layout(void);
 void dg_set_num_sms(int n);
 int dg_get_num_sms(void);
 
-/* Tail split of the dense, contiguous and masked forms, with either scale form (not the fused
-   SwiGLU, the K-grouped form or dg_fp8_gemm_nt_noalloc; calls whose configuration already splits K
-   are unaffected). When the output tiles of a launch
+/* Time limit, in microseconds, of every pipeline wait inside the kernels (a wait on a copy, an MMA or
+   a hand-over between warps). No wait of a working launch comes near the default of 2 s. A wait that
+   exceeds the limit sets DG_DEV_TIMEOUT in the device status word; the kernel then stops issuing work,
+   waits (with a fixed 2 s bound) for its copies and MMAs already in flight, frees its tensor memory and
+   returns, leaving the output undefined where it gave up; dg_get_device_status reports the bit and
+   clears the split-K counters, and the next call works normally. The limit applies to launches made
+   after the call. us < 0 restores the default; values above 16777215 (about 16.8 s) are clamped;
+   0 makes every wait that is not already satisfied give up at once (a way to exercise the recovery
+   path without a fault). The environment variable DG_WAIT_LIMIT_US sets the initial value. Returns
+   the previous value. The pages have no counterpart: this is part of this library's failure
+   detection. */
+long long dg_set_wait_limit_us(long long us);
+
+/* Tail split of the dense, contiguous and masked forms (dg_fp8_gemm_nt_noalloc included), with
+   either scale form (not the fused SwiGLU or the K-grouped form; calls whose configuration already
+   splits K are unaffected). When the output tiles of a launch
    leave a last, partial wave of at most half the grid, the kernel may cut each of those tiles into
    up to n K ranges, computed by otherwise idle SMs and summed in range order (deterministic) by the
    last range to finish, exactly as split-K does. The kernel takes the split only when its cost model

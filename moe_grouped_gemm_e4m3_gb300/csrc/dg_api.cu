@@ -85,6 +85,30 @@ int cluster_capacity(int mode, int block_n, bool out_f32, int splits, bool block
   return cache[dev][k][m][b][f][splits];
 }
 
+// Time limit of the kernels' pipeline waits, in microseconds, carried in bits 8..31 of the kernel
+// flags word: default 2 s; DG_WAIT_LIMIT_US sets the initial value, dg_set_wait_limit_us() changes it.
+constexpr long long kDefaultWaitLimitUs = 2000000;
+constexpr long long kMaxWaitLimitUs = (1LL << (32 - dg::kWaitLimitShift)) - 1;   // ~16.7 s
+std::atomic<long long> g_wait_limit_us{-1};   // -1: not yet initialised from DG_WAIT_LIMIT_US
+
+long long clamp_wait_limit(long long us) {
+  return us < 0 ? kDefaultWaitLimitUs : (us > kMaxWaitLimitUs ? kMaxWaitLimitUs : us);
+}
+
+long long wait_limit_setting() {
+  long long v = g_wait_limit_us.load();
+  if (v < 0) {
+    const char* e = std::getenv("DG_WAIT_LIMIT_US");
+    long long expected = -1;
+    g_wait_limit_us.compare_exchange_strong(expected, clamp_wait_limit(e ? std::atoll(e) : kDefaultWaitLimitUs));
+    v = g_wait_limit_us.load();
+  }
+  return v;
+}
+
+// The wait limit's bits of the kernel flags word.
+int wait_limit_flags() { return (int)((uint32_t)wait_limit_setting() << dg::kWaitLimitShift); }
+
 int tail_splits_setting() {
   int v = g_tail_splits.load();
   if (v < 0) {
@@ -339,15 +363,25 @@ dg_status ensure_workspace(DeviceState& st, size_t floats, size_t counters, cuda
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The allocation-free call's fixed split-K scratch: its capacity, and the device address of the
+// array on the current device (the array and this lookup are defined with the entry point at the end
+// of this file).
+constexpr size_t kNoAllocCounterBytes = 4096 * sizeof(int);   // 4096 output tiles
+constexpr size_t kNoAllocWorkspaceBytes = size_t(20) << 20;   // 20 MiB of FP32 partials
+dg_status noalloc_scratch(void** out);
+
 // Common implementation of the six GEMM entry points.
 //   mode dense: rows = M, G = 1;  contiguous: rows = M_total;  masked: rows = M_max (per group).
 //   sA/sB are FP32 scales, or (block_scaled) packed UE8M0 words: sA [G][ceil(nkb/4)][ldsa] and
 //   sB [G][nnb][ceil(nkb/4)] int32.
 //   C (dense, FP32 D only): D = C + A·Bᵀ. C may be D itself; otherwise it is copied into D first.
+//   noalloc (dense, BF16, FP32 scales only): split-K scratch comes from the fixed array of the
+//   allocation-free entry point instead of the lazily grown workspace; a shape that needs more
+//   than it holds returns DG_ERR_UNSUPPORTED.
 dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, const uint8_t* B, const void* sB,
                    const int32_t* idx, void* D, int rows, int N, int K, int G, cudaStream_t stream,
                    bool block_scaled = false, const float* C = nullptr, bool accumulate = false,
-                   bool swiglu = false, bool a_mn = false, bool b_mn = false) {
+                   bool swiglu = false, bool a_mn = false, bool b_mn = false, bool noalloc = false) {
   t_last_error.clear();
   if (rows < 0 || N < 0 || K < 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
   if (mode != dg::kDense && G < 1 && rows > 0) {
@@ -419,7 +453,8 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.num_m_blocks = ceil_div(rows, 128);
   p.num_n_blocks = swiglu ? d_cols / 128 : ceil_div(N, cfg.block_n);
   p.swiglu_i = swiglu ? d_cols : 0;
-  p.flags = (a_mn ? dg::kFlagAMN : 0) | (b_mn ? dg::kFlagBMN : 0) | (accumulate ? dg::kFlagAccumulate : 0);
+  p.flags = (a_mn ? dg::kFlagAMN : 0) | (b_mn ? dg::kFlagBMN : 0) | (accumulate ? dg::kFlagAccumulate : 0) |
+            wait_limit_flags();
   p.num_splits = cfg.splits;
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles;   // masked: counted on the device
@@ -450,9 +485,26 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
     const size_t floats = cfg.splits > 1 ? (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n
                                          : (size_t)cfg.grid * 128 * cfg.block_n;
     const size_t counters = cfg.splits > 1 ? (size_t)cfg.tiles : (size_t)cfg.grid;
-    if ((s = ensure_workspace(*st, floats, counters, stream)) != DG_OK) return s;
-    p.workspace = st->workspace;
-    p.counters = st->counters;
+    if (noalloc) {
+      if (counters * sizeof(int) > kNoAllocCounterBytes || floats * sizeof(float) > kNoAllocWorkspaceBytes)
+        return fail(DG_ERR_UNSUPPORTED,
+                    "dg_fp8_gemm_nt_noalloc: this shape needs " + std::to_string(floats * sizeof(float)) +
+                        " bytes of split-K partials and " + std::to_string(counters) + " counters; the fixed scratch holds " +
+                        std::to_string(kNoAllocWorkspaceBytes) + " bytes and " +
+                        std::to_string(kNoAllocCounterBytes / sizeof(int)) + " counters (use dg_fp8_gemm_nt)");
+      void* scratch = nullptr;
+      if ((s = noalloc_scratch(&scratch)) != DG_OK) return s;
+      unsigned char* base = static_cast<unsigned char*>(scratch);
+      p.counters = reinterpret_cast<int*>(base);
+      p.workspace = reinterpret_cast<float*>(base + kNoAllocCounterBytes);
+      // The array keeps whatever the previous call left; the arrival counters must start at zero.
+      const cudaError_t me = cudaMemsetAsync(p.counters, 0, counters * sizeof(int), stream);
+      if (me != cudaSuccess) return fail_cuda(me, "cudaMemsetAsync(noalloc counters)");
+    } else {
+      if ((s = ensure_workspace(*st, floats, counters, stream)) != DG_OK) return s;
+      p.workspace = st->workspace;
+      p.counters = st->counters;
+    }
   }
 
   if (a_mn) {   // A stored [K, M]: M contiguous
@@ -561,7 +613,7 @@ dg_status run_k_grouped(bool out_f32, const uint8_t* A, const float* sA, const u
   p.sB = sB;
   p.D = D;
   p.status = st->status;
-  p.flags = dg::kFlagAMN | dg::kFlagBMN;
+  p.flags = dg::kFlagAMN | dg::kFlagBMN | wait_limit_flags();
   p.m_indices = offsets;   // the K offsets of the groups
   if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)M, (uint64_t)K_total, (uint64_t)M, 128, 128,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
@@ -760,6 +812,12 @@ int dg_set_cluster_split(int on) {
   return prev;
 }
 
+long long dg_set_wait_limit_us(long long us) {
+  const long long prev = wait_limit_setting();
+  g_wait_limit_us.store(clamp_wait_limit(us));
+  return prev;
+}
+
 int dg_set_tail_splits(int n) {
   const int prev = tail_splits_setting();
   g_tail_splits.store(n > 0 ? clamp_tail_splits(n) : kTailSplits);
@@ -848,17 +906,9 @@ dg_status dg_query_config_ue8m0(int mode, int M, int N, int K, int G, int out_f3
 // dg_fp8_gemm_nt_noalloc serves them: the split-K partials and arrival counters live in the
 // fixed array below, which every device that loads libdg holds until the process exits.
 
-namespace {
-
-constexpr size_t kNoAllocCounterBytes = 4096 * sizeof(int);                 // 4096 output tiles
-constexpr size_t kNoAllocWorkspaceBytes = size_t(20) << 20;                 // 20 MiB of FP32 partials
-constexpr size_t kNoAllocScratchBytes = kNoAllocCounterBytes + kNoAllocWorkspaceBytes;
-
-}  // namespace
-
 // Layout: [counters: 4096 int][workspace: 20 MiB of float]. Shared by every call on a device.
 // Split-K uses at most one wave of 128x256 FP32 partial tiles (128 KiB each): 160 of them fit.
-static __device__ __align__(256) unsigned char g_dg_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) unsigned char g_dg_noalloc_scratch[kNoAllocCounterBytes + kNoAllocWorkspaceBytes];
 
 namespace {
 
@@ -887,89 +937,16 @@ dg_status noalloc_scratch(void** out) {
 
 }  // namespace
 
+// The allocation-free dense GEMM: the same validation, schedule and kernels as dg_fp8_gemm_nt (one
+// shared code path), with any split-K scratch taken from the fixed array above.
 extern "C" dg_status dg_fp8_gemm_nt_noalloc(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                                             uint16_t* D, int M, int N, int K, dg_stream_t stream) {
   t_last_error.clear();
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (M < 0 || N < 0 || K < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
-  if (M == 0 || N == 0) return DG_OK;
-  if (K == 0) return fail(DG_ERR_INVALID_ARG, "K must be positive");
-  if (!A || !sA || !B || !sB || !D) return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
-  if (K % 16 != 0) return fail(DG_ERR_ALIGNMENT, "K must be a multiple of 16 (16-byte rows of E4M3 A and B)");
-  if (N % 8 != 0) return fail(DG_ERR_ALIGNMENT, "N must be a multiple of 8 (16-byte rows of BF16 D)");
-  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(D, 16))
-    return fail(DG_ERR_ALIGNMENT, "A, B and D must be 16-byte aligned");
-  if (!aligned(sA, 4) || !aligned(sB, 4)) return fail(DG_ERR_ALIGNMENT, "sA and sB must be 4-byte aligned");
-  if (M > INT_MAX - 256 || N > INT_MAX - 256 || K > INT_MAX - 256)
-    return fail(DG_ERR_UNSUPPORTED, "a tensor extent exceeds 2^31 - 257");
-
-  DeviceState* st = nullptr;
-  dg_status s = device_state(&st);
-  if (s != DG_OK) return s;
+  // The array is looked up first, so that every call, even one that needs no scratch, performs the
+  // per-device set-up (the first call on a device belongs before any stream capture).
   void* scratch = nullptr;
-  if ((s = noalloc_scratch(&scratch)) != DG_OK) return s;
-
-  // The schedule of dg_fp8_gemm_nt: the same configuration, cluster split-K (which needs no
-  // scratch) and the tail split (one wave of partials at most), so that the two agree bit for bit.
-  Config cfg = choose_config(dg::kDense, M, N, K, 1, effective_sms(*st));
-  fit_cluster_splits(cfg, dg::kDense, K, false, false);
-  const bool cluster = use_cluster_split(cfg, dg::kDense, false, false, false);
-  const bool tail = !cluster && cfg.splits == 1 && tail_splits_setting() > 1;
-  const bool global_split = !cluster && cfg.splits > 1;
-  const size_t counter_bytes = (size_t)(tail ? cfg.grid : cfg.tiles) * sizeof(int);
-  const size_t partial_bytes = (size_t)(tail ? cfg.grid : cfg.tiles * cfg.splits) * 128 * cfg.block_n * sizeof(float);
-  if ((global_split || tail) && (counter_bytes > kNoAllocCounterBytes || partial_bytes > kNoAllocWorkspaceBytes))
-    return fail(DG_ERR_UNSUPPORTED,
-                "dg_fp8_gemm_nt_noalloc: this shape needs " + std::to_string(partial_bytes) + " bytes of split-K "
-                "partials and " + std::to_string(cfg.tiles) + " counters; the fixed scratch holds " +
-                std::to_string(kNoAllocWorkspaceBytes) + " bytes and 4096 counters (use dg_fp8_gemm_nt)");
-
-  dg::LaunchArgs a;
-  std::memset(&a, 0, sizeof(a));
-  dg::GemmParams& p = a.p;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.G = 1;
-  p.nkb = ceil_div(K, 128);
-  p.nnb = ceil_div(N, 128);
-  p.ldsa = dg_get_tma_aligned_size(M, 4);
-  p.num_m_blocks = ceil_div(M, 128);
-  p.num_n_blocks = ceil_div(N, cfg.block_n);
-  p.num_splits = cfg.splits;
-  p.kb_per_split = cfg.kb_per_split;
-  p.num_tiles = cfg.tiles;
-  p.raster_m = (int16_t)cfg.raster_m;
-  p.tail_splits = (int16_t)(tail ? tail_splits_setting() : 1);
-  p.sA = sA;
-  p.sB = sB;
-  p.D = D;
-  p.status = st->status;
-  if (cluster) {
-    p.flags |= dg::kFlagClusterSplit;
-    a.cluster = cfg.splits;
-  } else if (global_split || tail) {
-    unsigned char* base = static_cast<unsigned char*>(scratch);
-    p.counters = reinterpret_cast<int*>(base);
-    p.workspace = reinterpret_cast<float*>(base + kNoAllocCounterBytes);
-    // The array keeps whatever the previous call left; the arrival counters must start at zero.
-    cudaError_t e = cudaMemsetAsync(p.counters, 0, counter_bytes, cs);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(noalloc counters)");
-  }
-  if ((s = encode_2d(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, 128, 128,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != DG_OK)
-    return s;
-  if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, 128,
-                     (uint32_t)cfg.block_n, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
-    return s;
-  if ((s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2, 32, 32,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B)) != DG_OK)
-    return s;
-  a.block_n = cfg.block_n;
-  a.out_f32 = false;
-  a.grid = cfg.grid;
-  a.stream = cs;
-  const cudaError_t e = dg::launch_dense(a);
-  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
-  return DG_OK;
+  const dg_status s = noalloc_scratch(&scratch);
+  if (s != DG_OK) return s;
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  nullptr, false, false, false, false, true);
 }
