@@ -75,7 +75,7 @@ struct GemmParams {
   float* workspace;  // split-K partial tiles
   int* counters;     // split-K arrival counter per output tile (zero between calls)
   int* status;       // device status word
-  int flags;         // kFlag* bits below
+  int flags;         // kFlag* bits below; bits 8..31: wait limit in microseconds
   int swiglu_i;      // fused SwiGLU: I, the width of H; B holds 2I rows per group (gate, then up)
 };
 
@@ -88,6 +88,8 @@ constexpr int kFlagBMN = 0x4;         // dense layouts: B stored [K, N] (MN-majo
 // of a tile are the CTAs of one cluster (rank = split), and they reduce through distributed
 // shared memory instead of the global workspace.
 constexpr int kFlagClusterSplit = 0x8;
+// Bits 8..31 of the flags word hold the time limit of the pipeline waits in microseconds
+// (kWaitLimitShift, mbar_wait).
 
 struct Tile {
   int g;          // group
@@ -409,6 +411,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Plan::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 8);
+  // cluster split-K: set when an epilogue warp of this CTA ends without its partial (a skipped tile,
+  // or a wait that gave up); the cluster then leaves D untouched
+  volatile int* no_partial = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 12);
   volatile int* sched_smem = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 16);   // Sched, 4 ints
 
   const int warp = threadIdx.x / 32;
@@ -431,6 +436,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     }
     *abort_flag = 0;
     *last_flag = 0;
+    *no_partial = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -483,7 +489,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1;
-            ok = mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, p.status);
+            ok = mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, p.status, p.flags);
             if (!ok) break;
             uint8_t* sa = smem + s * Plan::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
@@ -559,8 +565,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             const uint32_t aph = (g / NBUF) & 1;
             // the stage's data first (normally there long before), then the TMEM buffer, whose
             // release by the epilogue is the round trip this wait is on
-            ok = mbar_wait(&full_bar[s], ph, abort_flag, p.status) &&
-                 mbar_wait(&tempty_bar[b], aph ^ 1, abort_flag, p.status);
+            ok = mbar_wait(&full_bar[s], ph, abort_flag, p.status, p.flags) &&
+                 mbar_wait(&tempty_bar[b], aph ^ 1, abort_flag, p.status, p.flags);
             if (!ok) break;
             tc_fence_after();
             const uint64_t soff = (uint64_t)((s * Plan::kStageBytes) >> 4);
@@ -666,7 +672,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         const float sa_nxt = fetch_sa(kb + 1), sb_nxt = fetch_sb(kb + 1);
         // All 32 lanes wait together: one warp-wide instruction stream, uniform by construction
         // (every lane sees the same barrier phase, timer value and abort flag).
-        if (!mbar_wait(&tfull_bar[b], aph, abort_flag, p.status)) { alive = false; break; }
+        if (!mbar_wait(&tfull_bar[b], aph, abort_flag, p.status, p.flags)) { alive = false; break; }
         tc_fence_after();
         if (active) {
           const uint32_t taddr =
@@ -741,7 +747,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         if (lane == 0) mbar_arrive(epi_arrive_bar);
         int ok = 1;
         if (warp == 0 && lane == 0) {
-          ok = mbar_wait(epi_arrive_bar, sk_it & 1, abort_flag, p.status);
+          ok = mbar_wait(epi_arrive_bar, sk_it & 1, abort_flag, p.status, p.flags);
           if (ok) {
             const int prev = atomicAdd(p.counters + tile.out_idx, 1);
             const int last = (prev == tile.splits - 1);
@@ -750,7 +756,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             mbar_arrive(epi_release_bar);
           }
         }
-        if (lane == 0 && ok) ok = mbar_wait(epi_release_bar, sk_it & 1, abort_flag, p.status);
+        if (lane == 0 && ok) ok = mbar_wait(epi_release_bar, sk_it & 1, abort_flag, p.status, p.flags);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();
         ++sk_it;
@@ -790,7 +796,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           const uint32_t xph = x_it & 1;
           ++x_it;
           if (cgrp == 1) {
-            ok = mbar_wait(&xempty_bar[quad], xph ^ 1, abort_flag, p.status);
+            ok = mbar_wait(&xempty_bar[quad], xph ^ 1, abort_flag, p.status, p.flags);
             if (!ok) break;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -802,7 +808,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             if (lane == 0) mbar_arrive(&xfull_bar[quad]);
             continue;
           }
-          ok = mbar_wait(&xfull_bar[quad], xph, abort_flag, p.status);
+          ok = mbar_wait(&xfull_bar[quad], xph, abort_flag, p.status, p.flags);
           if (!ok) break;
           float h[32];
 #pragma unroll
@@ -979,9 +985,16 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         for (int j = 0; j < EPI_COLS; j += 4)
           st_shared_v4(part + row_in_tile * kRowBytes + (cgrp * EPI_COLS + j) * 4, __float_as_uint(acc[j]),
                        __float_as_uint(acc[j + 1]), __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+      } else if (lane == 0) {
+        *no_partial = 1;
       }
       cluster_sync_all();
-      if (have_partial) {
+      // Sum only if every CTA of the cluster holds its partial: a CTA that gave up (a wait timed out)
+      // has none, and its stage buffers hold stale bytes that must not reach D.
+      bool complete = have_partial;
+      for (uint32_t r = 0; complete && r < cluster_nctarank(); ++r)
+        complete = ld_cluster_u32(cluster_map(smem_u32(const_cast<int*>(no_partial)), r)) == 0;
+      if (complete) {
         const int S = stash[7], g = stash[0], n_blk = stash[2], a_row = stash[5], rows = stash[6];
         const int rank = (int)cluster_ctarank();
         constexpr int kVec = BN / 4;                       // float4 per row

@@ -112,6 +112,9 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Plan::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 8);
+  // cluster split-K: set when an epilogue warp of this CTA ends without its partial (a skipped tile,
+  // or a wait that gave up); the cluster then leaves D untouched
+  volatile int* no_partial = reinterpret_cast<volatile int*>(smem + Plan::kMiscOff + 12);
   volatile int* desc_ring = reinterpret_cast<volatile int*>(smem + Plan::kDescOff);
 
   const int warp = threadIdx.x / 32;
@@ -137,6 +140,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     *last_flag = 0;
+    *no_partial = 0;
     fence_barrier_init();
   }
   if (warp == R::kProducerWarp && lane == 0) {
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
           for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1;
-            ok = mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, p.status);
+            ok = mbar_wait(&empty_bar[s], ph ^ 1, abort_flag, p.status, p.flags);
             if (!ok) break;
             uint8_t* sa = smem + s * Plan::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         int ok = 1;
         if (lane == 0) {
           // the epilogue has loaded the previous tile's accumulator
-          ok = mbar_wait(acc_empty_bar, (tile_it & 1) ^ 1, abort_flag, p.status);
+          ok = mbar_wait(acc_empty_bar, (tile_it & 1) ^ 1, abort_flag, p.status, p.flags);
           tc_fence_after();
           int cur_quad = -1;
           uint32_t slot = 0;
@@ -219,13 +223,13 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
             const int quad = kb >> 2;
             if (quad != cur_quad) {
               slot = sf_it % SLOTS;
-              ok = mbar_wait(&sf_full_bar[slot], (sf_it / SLOTS) & 1, abort_flag, p.status);
+              ok = mbar_wait(&sf_full_bar[slot], (sf_it / SLOTS) & 1, abort_flag, p.status, p.flags);
               if (!ok) break;
               cur_quad = quad;
             }
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1;
-            ok = mbar_wait(&full_bar[s], ph, abort_flag, p.status);
+            ok = mbar_wait(&full_bar[s], ph, abort_flag, p.status, p.flags);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       bool alive = true;
       auto post = [&](const Tile& tl, int end) -> bool {
         const uint32_t ds = desc_it % Plan::kDescSlots;
-        if (!mbar_wait(&desc_empty_bar[ds], ((desc_it / Plan::kDescSlots) & 1) ^ 1, abort_flag, p.status))
+        if (!mbar_wait(&desc_empty_bar[ds], ((desc_it / Plan::kDescSlots) & 1) ^ 1, abort_flag, p.status, p.flags))
           return false;
         if (lane == 0) {
           volatile int* d = desc_ring + ds * 8;
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
           const uint32_t b0 = __ldg(sfb_ptr + quad);
           const uint32_t b1 = has_nb1 ? __ldg(sfb_ptr + nkq + quad) : 0x7F7F7F7Fu;
           const uint32_t slot = sf_it % SLOTS;
-          if (!mbar_wait(&sf_empty_bar[slot], ((sf_it / SLOTS) & 1) ^ 1, abort_flag, p.status)) {
+          if (!mbar_wait(&sf_empty_bar[slot], ((sf_it / SLOTS) & 1) ^ 1, abort_flag, p.status, p.flags)) {
             alive = false;
             break;
           }
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       bool active;
       {
         const uint32_t ds = desc_it % Plan::kDescSlots;
-        if (!mbar_wait(&desc_full_bar[ds], (desc_it / Plan::kDescSlots) & 1, abort_flag, p.status)) {
+        if (!mbar_wait(&desc_full_bar[ds], (desc_it / Plan::kDescSlots) & 1, abort_flag, p.status, p.flags)) {
           alive = false;
           break;
         }
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       uint32_t accu[EPI_COLS];
       float* const acc = reinterpret_cast<float*>(accu);
 
-      if (!mbar_wait(acc_full_bar, tile_it & 1, abort_flag, p.status)) { alive = false; break; }
+      if (!mbar_wait(acc_full_bar, tile_it & 1, abort_flag, p.status, p.flags)) { alive = false; break; }
       ++tile_it;
       tc_fence_after();
       if (active) {
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         if (lane == 0) mbar_arrive(epi_arrive_bar);
         int ok = 1;
         if (warp == 0 && lane == 0) {
-          ok = mbar_wait(epi_arrive_bar, sk_it & 1, abort_flag, p.status);
+          ok = mbar_wait(epi_arrive_bar, sk_it & 1, abort_flag, p.status, p.flags);
           if (ok) {
             const int prev = atomicAdd(p.counters + tile.out_idx, 1);
             const int last = (prev == tile.splits - 1);
@@ -440,7 +444,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
             mbar_arrive(epi_release_bar);
           }
         }
-        if (lane == 0 && ok) ok = mbar_wait(epi_release_bar, sk_it & 1, abort_flag, p.status);
+        if (lane == 0 && ok) ok = mbar_wait(epi_release_bar, sk_it & 1, abort_flag, p.status, p.flags);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();
         ++sk_it;
@@ -555,8 +559,14 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       // keeps every CTA's shared memory in place until its peers have read it. Every thread of the
       // cluster reaches both barriers on every path.
       const uint32_t part = smem_u32(smem);
+      if (!have_partial && lane == 0) *no_partial = 1;
       cluster_sync_all();
-      if (have_partial) {
+      // Sum only if every CTA of the cluster holds its partial: a CTA that gave up (a wait timed out)
+      // has none, and its stage buffers hold stale bytes that must not reach D.
+      bool complete = have_partial;
+      for (uint32_t r = 0; complete && r < cluster_nctarank(); ++r)
+        complete = ld_cluster_u32(cluster_map(smem_u32(const_cast<int*>(no_partial)), r)) == 0;
+      if (complete) {
         const int S = stash[3] >> 16, g = stash[0], n_blk = stash[2], a_row = stash[5], rows = stash[6];
         const int rank = (int)cluster_ctarank();
         constexpr int kVec = BN / 4;                       // float4 per row

@@ -73,25 +73,34 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar_addr, uint32_
   return ok != 0;
 }
 
-// Time limit of every pipeline wait. No legitimate wait in these kernels comes near it; when it
-// is exceeded the kernel records DG_DEV_TIMEOUT, raises the CTA's abort flag and unwinds.
+// Bound of the drain waits on an abandoned path (the copies and MMAs already in flight): they do
+// not use the caller's limit below, so that in-flight work is always waited for.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kStatusTimeout = 0x4;
 // Longest hardware suspension of one try_wait inside mbar_wait (the time limit is still checked
 // between suspensions).
 constexpr uint32_t kSuspendHintNs = 1000000u;
+// The time limit of every pipeline wait travels in bits 8..31 of the kernel's flags word, in
+// microseconds (the host sets it; default 2 s, up to about 16.7 s). No legitimate wait comes near
+// the default; when a wait exceeds the limit, the kernel records DG_DEV_TIMEOUT, raises the CTA's
+// abort flag and unwinds.
+constexpr int kWaitLimitShift = 8;
 
 // Waits until the phase with the given parity of `bar` has completed. Returns false (and sets
-// *abort) if the CTA's abort flag is raised or the time limit passes; the caller then unwinds.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+// *abort) if the CTA's abort flag is raised or the time limit in `flags` passes; the caller then
+// unwinds. The limit is only read once the phase was not already complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                          int flags) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
+  const uint64_t limit_ns = (uint64_t)((uint32_t)flags >> kWaitLimitShift) * 1000ull;
+  // (a suspension never outlasts the limit, so that a short limit really ends the wait)
+  const uint32_t hint = limit_ns < kSuspendHintNs ? (uint32_t)limit_ns : kSuspendHintNs;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait_suspend(a, parity, kSuspendHintNs)) return true;
+    if (mbar_try_wait_suspend(a, parity, hint)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(status, kStatusTimeout);
       *abort = 1;
       return false;
@@ -119,6 +128,18 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {

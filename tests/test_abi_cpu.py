@@ -111,3 +111,16 @@ def test_cluster_split_setting_is_host_state():
         assert dg.dg_set_cluster_split(True) is True
     finally:
         dg.dg_set_cluster_split(prev)
+
+
+def test_wait_limit_setting():
+    """The kernels' wait limit is a host setting (no GPU needed): default 2 s, clamped to the 24-bit
+    microsecond field of the kernel flags word, -1 restores the default."""
+    prev = dg.dg_set_wait_limit_us(5000)
+    try:
+        assert dg.dg_set_wait_limit_us(10 ** 12) == 5000
+        assert dg.dg_set_wait_limit_us(-1) == (1 << 24) - 1
+        assert dg.dg_set_wait_limit_us(0) == 2000000
+        assert dg.dg_set_wait_limit_us(prev) == 0
+    finally:
+        dg.dg_set_wait_limit_us(prev)
