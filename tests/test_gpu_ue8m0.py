@@ -193,7 +193,10 @@ def test_ue8m0_contiguous_moe_sampled(dg, G, N, K):
     pa, pb, sA, sB = _packed(a, b)
     D, D32 = _run_contig(dg, a, pa, b, pb, m_idx)
     assert torch.equal(bits16(D).cpu(), rne_bf16_bits(D32))
-    ms, ns = boundary_samples(G * rows_per, N, 2000, seed=G * N, block_rows=rows_per, block_cols=256)
+    # group boundaries and edges, plus every 128 x 256 output tile
+    ms, ns = boundary_samples(G * rows_per, N, 2000, seed=G * N, block_rows=rows_per, block_cols=256, per_tile=0)
+    mt, nt = boundary_samples(G * rows_per, N, 0, seed=G * N + 1, block_rows=128, block_cols=256)
+    ms, ns = np.concatenate([ms, mt]), np.concatenate([ns, nt])
     ref = oracle.contiguous_sampled(a.A, sA, b.B, sB, m_idx, ms, ns)
     assert_accurate(D32.cpu().numpy()[ms, ns], bits16(D).cpu().numpy()[ms, ns], ref,
                     f"ue8m0 contiguous G={G} {N}x{K}")
