@@ -77,6 +77,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config entries (configs 1, 3, 4 and 5 timed after the sweep)")
     ap.add_argument("--cpu-sample", type=int, default=CPU_SAMPLE_PER_SHAPE)
     ap.add_argument("--all-configs", action="store_true",
                     help="time every workload configuration (dense small, sweep, contiguous, masked, stress) "
@@ -104,6 +106,7 @@ def load_peaks():
             pk = json.load(f)
         return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
                 "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "sm_mhz_median": (pk.get("clocks_under_load") or {}).get("sm_mhz_median"),
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
@@ -411,11 +414,25 @@ def run_ours(args, rank, world, local):
                  "kernel_achieved_all_launches": round(dom["flops"] / (dom["ms"] * 1e-3) / 1e12, 1),
                  "peak_source": f"{peaks['source']}: 2 x bf16_tflops (dense FP8 = 2x BF16 nominal)"})
 
+    clocks = sampler.summary(t0, t1) if sampler else None
+    # The measured peak was taken under the power cap at a lower SM clock than the bench usually
+    # runs at; the same peak scaled to the bench's median clock shows how much of the fraction is
+    # clock, not kernel (a tensor-bound kernel's rate scales with the SM clock; HBM does not).
+    pk_mhz = peaks.get("sm_mhz_median")
+    if roof["bound"] == "tensor" and pk_mhz and clocks and clocks.get("sm_mhz"):
+        scaled = fp8_peak * clocks["sm_mhz"] / pk_mhz
+        roof.update({"peak_sm_mhz": pk_mhz, "bench_sm_mhz": clocks["sm_mhz"],
+                     "peak_at_bench_clock": round(scaled, 1), "frac_at_bench_clock": round(roof["achieved"] / scaled, 4)})
+
+    per_config, per_config_s = None, None
+    if not args.no_per_config and world == 1:
+        tp = time.time()
+        per_config = per_config_measure(dg, max(3, min(args.steps, 10)))
+        per_config_s = round(time.time() - tp, 1)
+
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(problems, args.cpu_sample)
-
-    clocks = sampler.summary(t0, t1) if sampler else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -434,10 +451,101 @@ def run_ours(args, rank, world, local):
         "clocks": clocks,
         "gpu_launches": len(tensors) * args.steps,
         "per_shape": per_shape,
+        "per_config": per_config,
+        "per_config_wall_s": per_config_s,
     }
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def per_config_measure(dg, reps):
+    """The workload configurations other than the sweep, each timed like the sweep's GEMMs (CUDA
+    events around the launch, L2 flushed before each repetition, mean over `reps`): config 1 (dense
+    128x512x1024), config 3 (contiguous grouped, G = 4 and 8, 8192 rows a group), config 4 (masked
+    decode, G = 16, M_max = 256) and config 5 (Student-t inputs with outlier channels). Returns one
+    entry per shape: time, TFLOP/s, algorithmic GB/s, the binding roof and the fraction of it."""
+    import torch
+    import dg_inputs
+    peaks = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    flush = L2Flush()
+    out = []
+
+    def timeit(fn):
+        fn()
+        ts = []
+        for r in range(reps):
+            flush(r)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.mean(ts))
+
+    def add(config, shape, flops, nbytes, ms, cfg=None):
+        t_tc, t_hbm = flops / (fp8_peak * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9)
+        bound = "tensor" if t_tc >= t_hbm else "hbm"
+        tflops, gbs = flops / (ms * 1e-3) / 1e12, nbytes / (ms * 1e-3) / 1e9
+        frac = tflops / fp8_peak if bound == "tensor" else gbs / peaks["hbm_gbs"]
+        e = {"config": config, "shape": shape, "us": round(ms * 1e3, 2), "tflops": round(tflops, 1),
+             "gbs": round(gbs, 1), "bound": bound, "roof_frac": round(frac, 3)}
+        if cfg:
+            e.update({"block_n": cfg["block_n"], "splits": cfg["splits"]})
+        out.append(e)
+
+    def nks(K):
+        nkb = -(-K // 128)
+        return -(-nkb // 4) if UE8M0 else nkb
+
+    def dense(config, M, N, K, dist=dg_inputs.NORMAL, outliers=0.0):
+        a = dg_inputs.make_a(M, K, seed=0, dist=dist, outlier_frac=outliers, ue8m0=UE8M0)
+        b = dg_inputs.make_b(1, N, K, seed=0, dist=dist, ue8m0=UE8M0)
+        gsA, gsB = gpu_scales(a, b)
+        A, sA, B, sB = dev(a.A), dev(gsA), dev(b.B[0]), dev(gsB[0])
+        D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        gemm = gemm_entry(dg)
+        ms = timeit(lambda: gemm(A, sA, B, sB, D))
+        add(config, f"{M}x{N}x{K}", 2.0 * M * N * K, algorithmic_bytes(M, N, K), ms, query_config(dg, 0, M, N, K))
+
+    dense("1 dense small", 128, 512, 1024)
+    # config 3: the G = 4 problem is the first four groups of the G = 8 one
+    for (N, K) in ((4096, 7168), (7168, 2048)):
+        a8 = dg_inputs.make_a(8 * 8192, K, seed=0, ue8m0=UE8M0)
+        b8 = dg_inputs.make_b(8, N, K, seed=0, ue8m0=UE8M0)
+        gsA8, gsB8 = gpu_scales(a8, b8)
+        for G in (4, 8):
+            M = G * 8192
+            A, B = dev(a8.A[:M]), dev(b8.B[:G])
+            sA, sB = dev(np.ascontiguousarray(gsA8[:, :M])), dev(gsB8[:G])
+            idx = dev(np.repeat(np.arange(G, dtype=np.int32), 8192))
+            D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            gemm = gemm_entry(dg, "contiguous")
+            ms = timeit(lambda: gemm(A, sA, B, sB, idx, D))
+            nbytes = M * K + G * N * K + 4 * M * nks(K) + 4 * G * (-(-N // 128)) * nks(K) + 2 * M * N
+            add("3 contiguous", f"G={G} M={M} N={N} K={K}", 2.0 * M * N * K, nbytes, ms, query_config(dg, 1, M, N, K, G))
+            del A, B, D
+        del a8, b8
+    for (N, K) in ((4096, 7168), (7168, 2048)):
+        G, M_max = 16, 256
+        mm = dg_inputs.make_masked_m(G, M_max, seed=0)
+        a = dg_inputs.make_masked_a(G, M_max, K, seed=0, ue8m0=UE8M0)
+        b = dg_inputs.make_b(G, N, K, seed=0, ue8m0=UE8M0)
+        gsA, gsB = gpu_scales(a, b)
+        A, sA, B, sB, MM = dev(a.A), dev(gsA), dev(b.B), dev(gsB), dev(mm)
+        D = torch.empty(G, M_max, N, dtype=torch.bfloat16, device="cuda")
+        gemm = gemm_entry(dg, "masked")
+        ms = timeit(lambda: gemm(A, sA, B, sB, MM, D))
+        valid, active = int(mm.sum()), int((mm > 0).sum())
+        nbytes = valid * K + active * N * K + 4 * valid * nks(K) + 4 * G * (-(-N // 128)) * nks(K) + 2 * valid * N
+        add("4 masked", f"G=16 M_max=256 sum(masked_m)={valid} N={N} K={K}", 2.0 * valid * N * K, nbytes, ms,
+            query_config(dg, 2, M_max, N, K, G))
+    for (M, N, K) in ((4096, 2112, 7168), (4096, 576, 7168), (4096, 7168, 32768)):
+        dense("5 stress (Student-t, outliers)", M, N, K, dist=dg_inputs.STUDENT_T3, outliers=0.01)
+    return out
 
 
 def measure_e2e(dg, problems, args, stream):
@@ -539,8 +647,11 @@ def cpu_baseline(problems, per_shape):
         flops += 2.0 * K * len(ms)
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{per_shape} random output elements of each of the {len(plan)} sweep GEMMs "
-                      f"({flops / 1e9:.2f} GFLOP, {dt:.1f} s), FP64 two-level accumulation, std::thread"}
+            "extrapolated": True,
+            "sample": f"a rate extrapolated from a sample: {per_shape} random output elements of each of the "
+                      f"{len(plan)} sweep GEMMs ({flops / 1e9:.2f} GFLOP in {dt:.1f} s; the whole sweep would take "
+                      f"about {sum(2.0 * M * N * K for (M, N, K, a, b, ms, ns) in plan) / (flops / dt) / 60:.0f} "
+                      f"min), FP64 two-level accumulation, std::thread"}
 
 
 def run_reference(args, rank, world):
