@@ -317,6 +317,23 @@ long long dg_set_wait_limit_us(long long us);
    152 SMs. */
 int dg_set_tail_splits(int n);
 
+/* Pairs of CTAs sharing B tiles (dense and contiguous calls with FP32 scales and K-major operands,
+   BN = 256, no split-K, at least 256 rows). The CTAs run as clusters of two over pairs of 128-row
+   blocks that use the same B tile: each CTA loads its own A tile and half of the B tile, which TMA
+   multicasts into both CTAs' shared memory, so each SM pulls a third less operand data from L2 per
+   K-block. A contiguous pair whose two blocks belong to different groups loads each group's B tile
+   separately. Results are bit-identical with pairing on or off; only the schedule changes, and a
+   paired launch has no tail split. dg_query_config reports a paired configuration as block_m 256.
+   Pairing is off by default: on = 1 switches it on, on = 0 off; the environment variable
+   DG_PAIR_B=1 sets it on initially. Returns the previous setting. Measured on GB300, the kernel's
+   period per K-block is set by the FP32 promotion's round trip through the tensor memory, not by
+   the L2-to-SM feed that pairing relieves (about 62 B/cycle per SM with all SMs loading), so
+   pairing gains nothing there and costs the tail split (4096x7168x16384: 397 us single, 419 us
+   paired). The pages say only that the design moves its operands with TMA ("DeepSeek AI libera
+   DeepGEMM…", 7minutos.es, § "Detalles y beneficios técnicos"); sharing them through multicast is
+   this implementation's choice. */
+int dg_set_pair_b(int on);
+
 /* Split-K inside thread-block clusters (dense and contiguous forms, either scale form). When a call
    splits K (few output tiles) into at most 8 ranges and every tile's ranges fit on the GPU at once
    as one cluster of CTAs, the ranges reduce through distributed shared memory: partials in each

@@ -59,6 +59,22 @@ bool cluster_split_setting() {
   return v != 0;
 }
 
+// Pairs of CTAs sharing B tiles through TMA multicast (dense and contiguous, FP32 scales, BN = 256,
+// no split-K): off unless DG_PAIR_B=1 or dg_set_pair_b(1). Measured on GB300, the FP32-scale kernel
+// is bound by its per-K-block TMEM round trip, not by the L2 feed that pairing relieves, and paired
+// launches lose the tail split: 4096x7168x16384 397 us single, 419 us paired.
+std::atomic<int> g_pair_b{-1};
+bool pair_b_setting() {
+  int v = g_pair_b.load();
+  if (v < 0) {
+    const char* e = std::getenv("DG_PAIR_B");
+    int expected = -1;
+    g_pair_b.compare_exchange_strong(expected, (e && std::atoi(e) != 0) ? 1 : 0);
+    v = g_pair_b.load();
+  }
+  return v != 0;
+}
+
 // Largest cluster of the cluster split-K: the portable limit.
 constexpr int kMaxClusterSplit = 8;
 
@@ -70,7 +86,8 @@ int cluster_capacity(int mode, int block_n, bool out_f32, int splits, bool block
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   if (splits < 2 || splits > kMaxClusterSplit || (mode != dg::kDense && mode != dg::kContiguous)) return 0;
-  const int k = block_scaled ? 1 : 0, m = mode == dg::kDense ? 0 : 1, b = block_n == 256 ? 1 : 0, f = out_f32 ? 1 : 0;
+  const int k = block_scaled ? 1 : 0, m = mode == dg::kDense ? 0 : 1, f = out_f32 ? 1 : 0;
+  const int b = block_n == 256 ? 1 : 0;
   std::lock_guard<std::mutex> lock(mu);
   if (!have[dev][k][m][b][f][splits]) {
     int n;
@@ -314,6 +331,16 @@ bool use_cluster_split(const Config& c, int mode, bool out_f32, bool block_scale
          cluster_capacity(mode, c.block_n, out_f32, c.splits, block_scaled) >= c.tiles;
 }
 
+// Whether a call with this configuration runs as pairs of CTAs sharing B (kFlagPairB): dense or
+// contiguous with FP32 scales and K-major operands, BN = 256, no split-K, at least two 128-row
+// blocks, and clusters of 2 can be resident. Returns the resident clusters of 2 (0: no pairing).
+int pair_clusters(const Config& c, int mode, int rows, bool out_f32, bool block_scaled, bool swiglu, bool mn_layout) {
+  if (!pair_b_setting() || block_scaled || swiglu || mn_layout) return 0;
+  if ((mode != dg::kDense && mode != dg::kContiguous) || c.block_n != 256 || c.splits != 1 || ceil_div(rows, 128) < 2)
+    return 0;
+  return cluster_capacity(mode, 256, out_f32, 2, false);
+}
+
 // Read on every call (a debugging aid), so that a process can switch it on and off.
 bool print_configs() {
   const char* e = std::getenv("DG_PRINT_CONFIGS");
@@ -478,10 +505,24 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   // distributed shared memory (no workspace, no counters) when every tile's cluster can be resident
   // at once and each CTA gets exactly one work unit.
   const bool cluster = use_cluster_split(cfg, mode, out_f32, block_scaled, swiglu);
+  // Pairs of CTAs share B tiles (kFlagPairB): the persistent units are pairs of 128-row blocks by
+  // BN columns, walked by clusters of 2; no tail split.
+  const int pair_cap = cluster ? 0 : pair_clusters(cfg, mode, rows, out_f32, block_scaled, swiglu, a_mn || b_mn);
+  const bool pair = pair_cap > 0;
+  if (pair) {
+    const int m_pairs = ceil_div(ceil_div(rows, 128), 2);
+    const long long units = (long long)m_pairs * ceil_div(N, cfg.block_n);
+    p.flags |= dg::kFlagPairB;
+    p.num_tiles = (int)units;
+    p.raster_m = (int16_t)(m_pairs < 8 ? m_pairs : 8);
+    p.tail_splits = 1;
+    a.cluster = 2;
+    cfg.grid = 2 * (int)(units < pair_cap ? units : pair_cap);
+  }
   if (cluster) {
     p.flags |= dg::kFlagClusterSplit;
     a.cluster = cfg.splits;
-  } else if (cfg.splits > 1 || tail) {
+  } else if (!pair && (cfg.splits > 1 || tail)) {
     const size_t floats = cfg.splits > 1 ? (size_t)cfg.tiles * cfg.splits * 128 * cfg.block_n
                                          : (size_t)cfg.grid * 128 * cfg.block_n;
     const size_t counters = cfg.splits > 1 ? (size_t)cfg.tiles : (size_t)cfg.grid;
@@ -520,7 +561,8 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
                        128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK)
       return s;
   } else if ((s = encode_2d(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, (uint64_t)K, (uint64_t)b_rows, (uint64_t)K, 128,
-                            (uint32_t)(swiglu ? 128 : cfg.block_n), CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK) {
+                            (uint32_t)(swiglu ? 128 : (pair ? cfg.block_n / 2 : cfg.block_n)),
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK) {
     return s;
   }
   if (out_f32) {
@@ -540,7 +582,8 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
     static const char* names[3] = {"dense", "contiguous", "masked"};
     std::fprintf(stderr, "[dg] %s%s%s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d%s grid=%d tiles=%d\n",
                  names[mode], block_scaled ? "/ue8m0" : "", swiglu ? "/swiglu" : "", out_f32 ? "/f32" : "", rows, N, K,
-                 p.G, cfg.block_n, cfg.stages, cfg.splits, cluster ? " (cluster)" : "", cfg.grid, cfg.tiles);
+                 p.G, cfg.block_n, cfg.stages, cfg.splits, cluster ? " (cluster)" : (pair ? " (pairs sharing B)" : ""),
+                 cfg.grid, cfg.tiles);
   }
   cudaError_t e;
   if (swiglu) {
@@ -806,6 +849,12 @@ void dg_set_num_sms(int n) {
   g_num_sms_cap.store(n > 0 ? n : 0);
 }
 
+int dg_set_pair_b(int on) {
+  const int prev = pair_b_setting() ? 1 : 0;
+  g_pair_b.store(on ? 1 : 0);
+  return prev;
+}
+
 int dg_set_cluster_split(int on) {
   const int prev = cluster_split_setting() ? 1 : 0;
   g_cluster_split.store(on ? 1 : 0);
@@ -873,8 +922,18 @@ dg_status query_config(int mode, int M, int N, int K, int G, int* cfg, bool bloc
   if (device_state(&st) == DG_OK) sms = effective_sms(*st);
   if (sms <= 0) sms = 152;  // no device: report the GB300 configuration
   Config c = choose_config(mode, M, N, K, mode == 0 ? 1 : G, sms, block_scaled);
-  if (st) fit_cluster_splits(c, mode, K, block_scaled, false);
-  cfg[0] = 128;
+  int block_m = 128;
+  if (st) {
+    fit_cluster_splits(c, mode, K, block_scaled, false);
+    const int cap = use_cluster_split(c, mode, false, block_scaled, false)
+                        ? 0 : pair_clusters(c, mode, M, false, block_scaled, false, false);
+    if (cap > 0) {   // pairs of CTAs: 256 rows (two CTAs of 128) by BN columns per unit
+      const long long units = (long long)ceil_div(ceil_div(M, 128), 2) * ceil_div(N, c.block_n);
+      c.grid = 2 * (int)(units < cap ? units : cap);
+      block_m = 256;
+    }
+  }
+  cfg[0] = block_m;
   cfg[1] = c.block_n;
   cfg[2] = c.stages;
   cfg[3] = c.splits;

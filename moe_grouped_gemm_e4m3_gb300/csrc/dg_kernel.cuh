@@ -88,6 +88,11 @@ constexpr int kFlagBMN = 0x4;         // dense layouts: B stored [K, N] (MN-majo
 // of a tile are the CTAs of one cluster (rank = split), and they reduce through distributed
 // shared memory instead of the global workspace.
 constexpr int kFlagClusterSplit = 0x8;
+// Pairs of CTAs (clusters of 2) over pairs of 128-row blocks that use the same B tile (dense and
+// contiguous, BN = 256, no split-K): each CTA loads its own A tile and half of the B tile,
+// which TMA multicasts into both CTAs' shared memory, so each SM pulls a third less from L2 per
+// K-block. Every MMA commit then releases the stage in both CTAs (empty barriers count 2).
+constexpr int kFlagPairB = 0x10;
 // Bits 8..31 of the flags word hold the time limit of the pipeline waits in microseconds
 // (kWaitLimitShift, mbar_wait).
 
@@ -102,7 +107,14 @@ struct Tile {
   int rows;       // rows of the tile that exist for this group (<= 128)
   int kb0, kb1;   // K-block range
   bool skip;      // nothing to compute (all-padding block, bad group)
+  bool shared;    // pair mode: both CTAs of the pair use this B tile (each loads half of it)
 };
+
+// Pair mode: this CTA's rank in its cluster of 2 (0 otherwise). A 1-D cluster of 2 holds the blocks
+// 2c and 2c + 1.
+__device__ __forceinline__ int pair_rank(const GemmParams& p) {
+  return (p.flags & kFlagPairB) ? (int)(blockIdx.x & 1) : 0;
+}
 
 // ---------------------------------------------------------------------------------------------
 // Tile scheduling. Every role walks the same sequence of linear tile ids (blockIdx.x, then +grid)
@@ -182,6 +194,7 @@ template <int BN, Mode MODE>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Sched& sc, int t, int lane) {
   Tile tile;
   tile.skip = false;
+  tile.shared = false;
   int u;   // output tile
   if (t < sc.whole) {
     u = t;
@@ -245,34 +258,52 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const Sched& sc
       tile.g = u / tiles_per_group;
       v = u - tile.g * tiles_per_group;
     }
+    // pair mode: the rasterised unit is a pair of m-blocks (2j, 2j+1), rank r of the cluster takes 2j+r
+    const bool pair = BN == 256 && (MODE == kDense || MODE == kContiguous) && (p.flags & kFlagPairB);
+    const int m_units = pair ? (p.num_m_blocks + 1) / 2 : p.num_m_blocks;
     const int per_group = p.raster_m * p.num_n_blocks;
     const int grp = v / per_group;
     const int first_m = grp * p.raster_m;
-    const int gsz = min(p.num_m_blocks - first_m, p.raster_m);
+    const int gsz = min(m_units - first_m, p.raster_m);
     const int local = v % per_group;
-    tile.m_blk = first_m + local % gsz;
+    const int m_unit = first_m + local % gsz;
+    tile.m_blk = pair ? 2 * m_unit + (int)(blockIdx.x & 1) : m_unit;
     tile.n_blk = local / gsz;
     tile.a_row = tile.m_blk * 128;
-    tile.rows = min(128, p.M - tile.a_row);
+    tile.rows = min(128, p.M - tile.a_row);   // pair mode: <= 0 for a second block past M
+    tile.shared = pair;
     if constexpr (MODE != kKGrouped) tile.g = 0;
     if constexpr (MODE == kContiguous) {
-      // The block's group is the largest valid index among its rows (padding rows are -1).
+      // A block's group is the largest valid index among its rows (padding rows are -1).
       // Rows with an index outside [-1, G) are flagged and never stored.
-      int mx = -1;
-      bool bad = false;
+      auto block_group = [&](int m_blk) -> int {
+        int mx = -1;
+        bool bad = false;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = tile.a_row + lane * 4 + i;
-        if (r < p.M) {
-          const int idx = __ldg(p.m_indices + r);
-          if (idx >= 0 && idx < p.G) mx = max(mx, idx);
-          bad |= (idx < -1 || idx >= p.G);
+        for (int i = 0; i < 4; ++i) {
+          const int r = m_blk * 128 + lane * 4 + i;
+          if (r < p.M) {
+            const int idx = __ldg(p.m_indices + r);
+            if (idx >= 0 && idx < p.G) mx = max(mx, idx);
+            bad |= (idx < -1 || idx >= p.G);
+          }
         }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kStatusBadGroup);
+        return (int)__reduce_max_sync(0xffffffffu, (unsigned)(mx + 1)) - 1;
+      };
+      if (pair) {
+        // Both CTAs of the pair decide alike: they share B when the two blocks have one group (or
+        // one of them is all padding, which computes with the other's B and stores nothing);
+        // otherwise each loads its own group's whole B tile. Nothing to do when both are padding.
+        const int g0 = block_group(2 * m_unit), g1 = block_group(2 * m_unit + 1);
+        const int g_own = (blockIdx.x & 1) ? g1 : g0, g_other = (blockIdx.x & 1) ? g0 : g1;
+        tile.g = g_own >= 0 ? g_own : g_other;
+        tile.shared = g0 < 0 || g1 < 0 || g0 == g1;
+        if (g0 < 0 && g1 < 0) tile.skip = true;
+      } else {
+        tile.g = block_group(tile.m_blk);
+        if (tile.g < 0) tile.skip = true;        // all padding (or all invalid): nothing to do
       }
-      const int g = (int)__reduce_max_sync(0xffffffffu, (unsigned)(mx + 1)) - 1;
-      tile.g = g;
-      if (g < 0) tile.skip = true;               // all padding (or all invalid): nothing to do
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kStatusBadGroup);
     }
     if constexpr (MODE == kKGrouped) {
       // the group's K-block range; an empty range still stores its (zero) tile. Offsets that are
@@ -314,7 +345,8 @@ struct Roles {
   // With more than 8 warps the launch budget is too small for 128 accumulators per epilogue
   // thread: shift registers from the producer/MMA warpgroup (56) to the epilogue warpgroups.
   static constexpr bool kRebalance = kThreads > 256;
-  static constexpr int kOtherRegs = 56;
+  // (BN = 128 epilogue warps hold 64 accumulators, so the producer and MMA warps get more there)
+  static constexpr int kOtherRegs = BN == 128 ? 80 : 56;
   static constexpr int kEpiRegs = ((kLaunchRegs * kThreads - kOtherRegs * 128) / kEpiThreads) / 8 * 8;
   static_assert(!kRebalance || kEpiRegs * kEpiThreads + kOtherRegs * 128 <= kLaunchRegs * kThreads,
                 "register split exceeds the launch budget");
@@ -419,10 +451,15 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
+  // pair mode (dense and contiguous, BN = 256): see kFlagPairB
+  const bool pair = (BN == 256 && (MODE == kDense || MODE == kContiguous) && !SWIGLU) && (p.flags & kFlagPairB);
+  // the persistent loop's first unit and stride: a pair walks the units together
+  const int unit0 = pair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustep = pair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], pair ? 2 : 1);   // pair mode: released by the MMAs of both CTAs
     }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(&tfull_bar[b], 1);
@@ -463,6 +500,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // pair mode: the peer's multicast copies and MMA commits arrive on this CTA's barriers, so both
+  // CTAs' barriers are initialised before either starts
+  if (pair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -479,7 +519,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
       const uint64_t policy = l2_policy_evict_last();
-      for (int t = blockIdx.x; alive && t < total_units; t += gridDim.x) {
+      for (int t = unit0; alive && t < total_units; t += ustep) {
         const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
         const int b_row = (MODE == kKGrouped ? 0 : tile.g * p.N) + tile.n_blk * BN;
@@ -509,6 +549,17 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
               tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, gate_row, policy);
               tma_load_2d(&tmB, sa + Plan::kABytes + 128 * 128, &full_bar[s], kb * 128, gate_row + p.swiglu_i,
                           policy);
+            } else if (BN == 256 && pair) {
+              // B's tensor map box is BN/2 rows here: the tile is two boxes, BN/2 x 128 bytes apart
+              constexpr int kHalf = BN / 2;
+              if (tile.shared) {
+                const int r = (int)(blockIdx.x & 1);   // this CTA's half, written into both CTAs
+                tma_load_2d_multicast(&tmB, sa + Plan::kABytes + r * kHalf * 128, &full_bar[s], kb * 128,
+                                      b_row + r * kHalf, (uint16_t)0x3, policy);
+              } else {
+                tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
+                tma_load_2d(&tmB, sa + Plan::kABytes + kHalf * 128, &full_bar[s], kb * 128, b_row + kHalf, policy);
+              }
             } else {
               tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
             }
@@ -525,6 +576,25 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           const uint32_t a = smem_u32(&full_bar[s]);
           const uint64_t t0 = global_timer_ns();
           while (!mbar_try_wait(a, (uint32_t)issued_phase[s]) && global_timer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+      if (pair && lane == 0) {
+        if (alive) {
+          // Both CTAs' MMAs have released this CTA's last stages: the peer's last commits have
+          // arrived on this CTA's barriers (and its copies into this CTA landed before them).
+          for (int s = 0; s < STAGES; ++s) {
+            if (issued_phase[s] < 0) continue;
+            const uint32_t a = smem_u32(&empty_bar[s]);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(a, (uint32_t)issued_phase[s]) && global_timer_ns() - t0 < kWaitLimitNs) {
+            }
+          }
+        } else {
+          // Abandoned: the peer may have issued copies into this CTA for stages this CTA never
+          // armed; give any such copy in flight time to land before the pair's final barrier.
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 50000ull) {
           }
         }
       }
@@ -551,7 +621,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       bool alive = true;
       int last_b = -1;
       uint32_t last_ph = 0;
-      for (int t = blockIdx.x; alive && t < total_units; t += gridDim.x) {
+      for (int t = unit0; alive && t < total_units; t += ustep) {
         const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
         const uint32_t nk = (uint32_t)(tile.kb1 - tile.kb0);
@@ -576,7 +646,10 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             for (int k = 0; k < 4; ++k) {
               mma_e4m3(d_tmem, adesc + a_step * k, bdesc + b_step * k, idesc, k > 0 ? 1u : 0u);
             }
-            mma_commit(&empty_bar[s]);
+            if (pair)
+              mma_commit_multicast(&empty_bar[s], (uint16_t)0x3);   // the stage is free in both CTAs' view
+            else
+              mma_commit(&empty_bar[s]);
             mma_commit(&tfull_bar[b]);
             last_b = b;
             last_ph = aph;
@@ -621,7 +694,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     float* const acc = reinterpret_cast<float*>(acc2);
 
     bool have_partial = false;   // cluster split: this CTA's partial tile is in acc
-    for (int t = blockIdx.x; alive && t < stash[11]; t += gridDim.x) {
+    for (int t = unit0; alive && t < stash[11]; t += ustep) {
       int kb_begin, kb_end;
       {
         const Sched sc = {stash[8], stash[9], stash[10], stash[11]};
@@ -1038,6 +1111,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   // ------------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  // pair mode: neither CTA leaves while its peer may still copy into it or arrive on its barriers
+  if (pair) cluster_sync_all();
   if (warp == R::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);

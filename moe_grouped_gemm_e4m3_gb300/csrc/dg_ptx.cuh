@@ -169,6 +169,18 @@ __device__ __forceinline__ void tma_load_2d(const void* tmap, void* smem_dst, ui
       : "memory");
 }
 
+// As tma_load_2d, but the box is written to the same shared-memory offset in every CTA of the
+// cluster named in `cta_mask`, and each of those CTAs' barrier at `bar`'s offset receives the
+// transaction bytes (this GPU's own memory only).
+__device__ __forceinline__ void tma_load_2d_multicast(const void* tmap, void* smem_dst, uint64_t* bar, int x, int y,
+                                                      uint16_t cta_mask, uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask), "l"(cache_policy)
+      : "memory");
+}
+
 // 2-D tiled store of a shared-memory box to global memory at (x, y); elements outside the
 // tensor's bounds are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_src, int x, int y) {
@@ -294,6 +306,15 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
+               : "memory");
+}
+
+// As mma_commit, but the arrival goes to the barrier at `bar`'s offset in every CTA of the cluster
+// named in `cta_mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(cta_mask)
                : "memory");
 }
 

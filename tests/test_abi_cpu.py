@@ -124,3 +124,13 @@ def test_wait_limit_setting():
         assert dg.dg_set_wait_limit_us(prev) == 0
     finally:
         dg.dg_set_wait_limit_us(prev)
+
+
+def test_pair_b_setting():
+    prev = dg.dg_set_pair_b(False)
+    assert prev is False                      # off by default (DG_PAIR_B unset)
+    try:
+        assert dg.dg_set_pair_b(True) is False
+        assert dg.dg_set_pair_b(prev) is True
+    finally:
+        dg.dg_set_pair_b(prev)

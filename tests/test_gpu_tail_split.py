@@ -27,7 +27,10 @@ def dg():
     import moe_grouped_gemm_e4m3_gb300 as m
     m.load()
     assert torch.cuda.is_available(), "GPU tests need CUDA"
+    # a launch by pairs of CTAs sharing B tiles has no tail split: these tests use single CTAs
+    prev = m.dg_set_pair_b(False)
     yield m
+    m.dg_set_pair_b(prev)
     assert m.dg_get_device_status() == 0
 
 

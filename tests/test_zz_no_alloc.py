@@ -82,14 +82,27 @@ def test_noalloc_split_k_through_the_array(dg, global_split_k, M, N, K):
 def test_noalloc_tail_split_through_the_array(dg):
     # 512 tiles on 152 SMs leave a last wave of 56 tiles (at most half the grid): the kernel cuts
     # them along K, and their partials go through the fixed array
+    # (single CTAs: a launch by pairs of CTAs sharing B tiles has no tail split)
     M, N, K = 4096, 4096, 7168
-    cfg = dg.dg_query_config(0, M, N, K)
-    assert cfg["splits"] == 1 and 0 < cfg["tiles"] % cfg["grid"] <= cfg["grid"] // 2, cfg
+    prev_pair = dg.dg_set_pair_b(False)
     prev = dg.dg_set_tail_splits(4)
     try:
+        cfg = dg.dg_query_config(0, M, N, K)
+        assert cfg["splits"] == 1 and 0 < cfg["tiles"] % cfg["grid"] <= cfg["grid"] // 2, cfg
         _check_twice(dg, M, N, K, seed=7)
     finally:
         dg.dg_set_tail_splits(prev)
+        dg.dg_set_pair_b(prev_pair)
+
+
+def test_noalloc_pairs_sharing_b(dg):
+    # pairs of CTAs sharing B tiles (opt-in): no scratch
+    prev = dg.dg_set_pair_b(True)
+    try:
+        assert dg.dg_query_config(0, 4096, 2112, 1024)["block_m"] == 256
+        _check_twice(dg, 4096, 2112, 1024, seed=11)
+    finally:
+        dg.dg_set_pair_b(prev)
 
 
 def test_noalloc_needs_no_scratch(dg):
