@@ -1064,9 +1064,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       cluster_sync_all();
       // Sum only if every CTA of the cluster holds its partial: a CTA that gave up (a wait timed out)
       // has none, and its stage buffers hold stale bytes that must not reach D.
-      bool complete = have_partial;
-      for (uint32_t r = 0; complete && r < cluster_nctarank(); ++r)
-        complete = ld_cluster_u32(cluster_map(smem_u32(const_cast<int*>(no_partial)), r)) == 0;
+      const bool complete = cluster_all_zero_u32(smem_u32(const_cast<int*>(no_partial))) && have_partial;
       if (complete) {
         const int S = stash[7], g = stash[0], n_blk = stash[2], a_row = stash[5], rows = stash[6];
         const int rank = (int)cluster_ctarank();
@@ -1075,11 +1073,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
         const int c4 = threadIdx.x % kVec;
         const int n = n_blk * BN + c4 * 4;
         for (int r = rank + (threadIdx.x / kVec) * S; r < rows; r += kRowsPerPass * S) {
-          float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          for (int s = 0; s < S; ++s) {
-            const float4 v = ld_cluster_v4(cluster_map(part + r * kRowBytes + c4 * 16, (uint32_t)s));
-            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
-          }
+          float4 tot = cluster_sum_v4(part + r * kRowBytes + c4 * 16, S);
           if (n >= p.N) continue;
           const size_t d_row = (size_t)(a_row + r);
           if constexpr (MODE == kContiguous) {

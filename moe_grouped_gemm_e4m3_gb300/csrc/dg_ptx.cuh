@@ -151,6 +151,41 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
   return v;
 }
 
+// Largest cluster the split-K exchange uses (the portable cluster size).
+constexpr int kMaxClusterCtas = 8;
+
+// True if the u32 at `addr` (an address in this CTA's shared memory) is 0 in every CTA of the
+// cluster. All the loads are in flight together, so the check costs one round trip through
+// distributed shared memory rather than one per CTA.
+__device__ __forceinline__ bool cluster_all_zero_u32(uint32_t addr) {
+  const uint32_t n = cluster_nctarank();
+  uint32_t v[kMaxClusterCtas];
+#pragma unroll
+  for (int r = 0; r < kMaxClusterCtas; ++r) v[r] = (uint32_t)r < n ? ld_cluster_u32(cluster_map(addr, (uint32_t)r)) : 0u;
+  uint32_t any = 0;
+#pragma unroll
+  for (int r = 0; r < kMaxClusterCtas; ++r) any |= v[r];
+  return any == 0;
+}
+
+// The sum over cluster ranks 0..S-1 (S <= kMaxClusterCtas) of the float4 at `addr` in each CTA's
+// shared memory, added in rank order starting from zero. The S loads are issued before the first
+// add, so they overlap instead of each waiting for the previous one.
+__device__ __forceinline__ float4 cluster_sum_v4(uint32_t addr, int S) {
+  float4 v[kMaxClusterCtas];
+#pragma unroll
+  for (int s = 0; s < kMaxClusterCtas; ++s)
+    if (s < S) v[s] = ld_cluster_v4(cluster_map(addr, (uint32_t)s));
+  float4 tot = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+  for (int s = 0; s < kMaxClusterCtas; ++s) {
+    if (s < S) {
+      tot.x += v[s].x; tot.y += v[s].y; tot.z += v[s].z; tot.w += v[s].w;
+    }
+  }
+  return tot;
+}
+
 // ---------------------------------------------------------------------------------------------
 // TMA (tensor maps are __grid_constant__ kernel parameters)
 
