@@ -253,9 +253,10 @@ dg_status dg_fp8_gemm_nt_ue8m0_acc_f32(const uint8_t* A, const int32_t* sA, cons
 /*
  * Allocation-free dense GEMM: the same computation, arguments and result as dg_fp8_gemm_nt (the
  * same validation, kernel, tile configuration, schedule and accumulation order: both entry points
- * run one code path, which differs only in where split-K scratch comes from), for callers that cannot let a library
- * call cudaMalloc — for example a framework whose caching allocator already owns the device memory,
- * or a serving loop that must not block on the device synchronisation cudaMalloc/cudaFree may do.
+ * run one code path, which differs only in where split-K scratch comes from), for callers that
+ * cannot let a library call cudaMalloc — for example a framework whose caching allocator already
+ * owns the device memory, or a serving loop that must not block on the device synchronisation
+ * cudaMalloc/cudaFree may do.
  * The DeepGEMM pages have no counterpart to this call; it is an addition of this library.
  *   - It allocates nothing. The split-K partials and arrival counters it may need live in one fixed
  *     array inside libdg (20 MiB of FP32 partials + 4096 counters, about 20.02 MiB), which every
@@ -325,13 +326,14 @@ int dg_set_tail_splits(int n);
    separately. Results are bit-identical with pairing on or off; only the schedule changes, and a
    paired launch has no tail split. dg_query_config reports a paired configuration as block_m 256.
    Pairing is off by default: on = 1 switches it on, on = 0 off; the environment variable
-   DG_PAIR_B=1 sets it on initially. Returns the previous setting. Measured on GB300, the kernel's
-   period per K-block is set by the FP32 promotion's round trip through the tensor memory, not by
-   the L2-to-SM feed that pairing relieves (about 62 B/cycle per SM with all SMs loading), so
-   pairing gains nothing there and costs the tail split (4096x7168x16384: 397 us single, 419 us
-   paired). The pages say only that the design moves its operands with TMA ("DeepSeek AI libera
-   DeepGEMM…", 7minutos.es, § "Detalles y beneficios técnicos"); sharing them through multicast is
-   this implementation's choice. */
+   DG_PAIR_B=1 sets it on initially. Returns the previous setting. Measured on GB300, pairing does
+   not shorten the kernel's period per K-block: that is set by the hand-off MMA -> promotion -> MMA
+   through the tensor memory, and each SM still receives the whole B tile. Pairing also loses the
+   tail split (4096x7168x16384: 397 us single, 419 us paired; under a sustained load the paired
+   launch draws less power and runs about 4% higher in clock, but needs about 8% more cycles).
+   The pages say only that the design moves its operands with TMA ("DeepSeek AI libera DeepGEMM…",
+   7minutos.es, § "Detalles y beneficios técnicos"); sharing them through multicast is this
+   implementation's choice. */
 int dg_set_pair_b(int on);
 
 /* Split-K inside thread-block clusters (dense and contiguous forms, either scale form). When a call
