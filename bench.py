@@ -831,17 +831,18 @@ def run_all_configs(args):
             report("7 masked + SwiGLU (fused)", f"G=16 M_max=256 sum(masked_m)={valid} 2I={N2} K={K}",
                    2.0 * valid * N2 * K, nbytes, ms, dict(scales))
             del A, B, H
-    # the NN / TN / TT layouts (FP32 scales only): A stored [K,M] and/or B stored [K,N]
-    if not UE8M0 and want(8):
+    # the NN / TN / TT layouts (both scale forms): A stored [K,M] and/or B stored [K,N]
+    if want(8):
         M, N, K = 4096, 7168, 2048
-        a = dg_inputs.make_a(M, K, seed=0)
-        b = dg_inputs.make_b(1, N, K, seed=0)
+        a = dg_inputs.make_a(M, K, seed=0, ue8m0=UE8M0)
+        b = dg_inputs.make_b(1, N, K, seed=0, ue8m0=UE8M0)
+        gsA, gsB = gpu_scales(a, b)
         for layout, (a_t, b_t) in (("nn", (False, True)), ("tn", (True, True)), ("tt", (True, False))):
             A = dev(np.ascontiguousarray(a.A.T) if a_t else a.A)
             B = dev(np.ascontiguousarray(b.B[0].T) if b_t else b.B[0])
-            sA, sB = dev(a.sA), dev(b.sB[0])
+            sA, sB = dev(gsA), dev(gsB[0])
             D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-            fn = getattr(dg, f"dg_fp8_gemm_{layout}")
+            fn = getattr(dg, f"dg_fp8_gemm_{layout}_ue8m0" if UE8M0 else f"dg_fp8_gemm_{layout}")
             ms = timeit(lambda: fn(A, sA, B, sB, D, M, N, K))
             report(f"8 layout {layout}", f"{M}x{N}x{K}", 2.0 * M * N * K, algorithmic_bytes(M, N, K), ms,
                    dict(scales, cfg=query_config(dg, 0, M, N, K)))

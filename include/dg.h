@@ -193,6 +193,25 @@ dg_status dg_fp8_gemm_tt(const uint8_t* A, const float* sA, const uint8_t* B, co
 dg_status dg_fp8_gemm_tt_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D,
                              int M, int N, int K, dg_stream_t stream);
 
+/* The NN, TN and TT layouts with power-of-two scales packed as UE8M0 (the block-scaled kernel):
+   the storage of A and B as for dg_fp8_gemm_nn / _tn / _tt, the packed scale layouts of
+   dg_fp8_gemm_nt_ue8m0 (sA [ceil(ceil(K/128)/4)][align4(M)], sB [ceil(N/128)][ceil(ceil(K/128)/4)]).
+   Each gives the NT call's result bit for bit. The pages list the four layouts for the SM100
+   implementation, which takes packed UE8M0 scales (same page, § "GEMM arayüzü ve yerleşim
+   kısıtları"). */
+dg_status dg_fp8_gemm_nn_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                               uint16_t* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_nn_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                   float* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_tn_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                               uint16_t* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_tn_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                   float* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_tt_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                               uint16_t* D, int M, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_gemm_tt_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                   float* D, int M, int N, int K, dg_stream_t stream);
+
 /*
  * K-grouped contiguous GEMM (MoE weight backward): grouped along K, with M and N shared by the groups
  * (k_grouped_fp8_gemm_tn_contiguous, tr.news.hada.io/topic?id=19459, § "Dense ve Grouped GEMM").

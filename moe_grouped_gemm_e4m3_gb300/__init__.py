@@ -42,6 +42,7 @@ __all__ = [
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
+    "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32",
     "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
     "DG_DEV_TIMEOUT",
@@ -62,6 +63,7 @@ EXPORTED_SYMBOLS = (
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
+    "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32",
     "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32",
 )
 
@@ -89,7 +91,7 @@ def load(build_if_missing: bool = True):
     P, i32 = ctypes.c_void_p, ctypes.c_int
     for name in ("dg_fp8_gemm_nt", "dg_fp8_gemm_nt_f32", "dg_fp8_gemm_nt_noalloc", "dg_fp8_gemm_nt_ue8m0",
                  "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32", "dg_fp8_gemm_tn",
-                 "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32"):
+                 "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32", "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, i32, i32, i32, P]
     for name in ("dg_fp8_grouped_contiguous", "dg_fp8_grouped_contiguous_f32", "dg_fp8_grouped_contiguous_ue8m0",
@@ -344,14 +346,16 @@ _LAYOUTS = {"nn": (False, True), "tn": (True, True), "tt": (True, False)}
 def _dense_layout(name, f32, A, sA, B, sB, D, M, N, K, stream):
     a_t, b_n = _LAYOUTS[name[len("dg_fp8_gemm_"):len("dg_fp8_gemm_") + 2]]
     M, N, K = int(M), int(N), int(K)
+    nks = _scale_k(name, K)
     _expect(A, "A", (K, M) if a_t else (M, K))
     _expect(B, "B", (K, N) if b_n else (N, K))
-    _expect(sA, "sA", (_cdiv(K, 128), _align4(M)))
-    _expect(sB, "sB", (_cdiv(N, 128), _cdiv(K, 128)))
+    _expect(sA, "sA", (nks, _align4(M)))
+    _expect(sB, "sB", (_cdiv(N, 128), nks))
     _expect(D, "D", (M, N))
     lib = load()
-    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
-                              _ptr(sB, "sB", _f32()), _ptr(D, "D", _d_types(f32)), M, N, K, _stream(stream)))
+    st = _scale_types(name)
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", st), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", st), _ptr(D, "D", _d_types(f32)), M, N, K, _stream(stream)))
     return D
 
 
@@ -380,6 +384,33 @@ def dg_fp8_gemm_tt(A, sA, B, sB, D, M, N, K, stream=None):
 
 def dg_fp8_gemm_tt_f32(A, sA, B, sB, D, M, N, K, stream=None):
     return _dense_layout("dg_fp8_gemm_tt_f32", True, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_nn_ue8m0(A, sA, B, sB, D, M, N, K, stream=None):
+    """dg_fp8_gemm_nn with packed UE8M0 scales (sA [ceil(nkb/4), align4(M)], sB [ceil(N/128), ceil(nkb/4)] int32)."""
+    return _dense_layout("dg_fp8_gemm_nn_ue8m0", False, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_nn_ue8m0_f32(A, sA, B, sB, D, M, N, K, stream=None):
+    return _dense_layout("dg_fp8_gemm_nn_ue8m0_f32", True, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_tn_ue8m0(A, sA, B, sB, D, M, N, K, stream=None):
+    """dg_fp8_gemm_tn with packed UE8M0 scales."""
+    return _dense_layout("dg_fp8_gemm_tn_ue8m0", False, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_tn_ue8m0_f32(A, sA, B, sB, D, M, N, K, stream=None):
+    return _dense_layout("dg_fp8_gemm_tn_ue8m0_f32", True, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_tt_ue8m0(A, sA, B, sB, D, M, N, K, stream=None):
+    """dg_fp8_gemm_tt with packed UE8M0 scales."""
+    return _dense_layout("dg_fp8_gemm_tt_ue8m0", False, A, sA, B, sB, D, M, N, K, stream)
+
+
+def dg_fp8_gemm_tt_ue8m0_f32(A, sA, B, sB, D, M, N, K, stream=None):
+    return _dense_layout("dg_fp8_gemm_tt_ue8m0_f32", True, A, sA, B, sB, D, M, N, K, stream)
 
 
 def _k_grouped(name, f32, A, sA, B, sB, k_offsets, D, stream):

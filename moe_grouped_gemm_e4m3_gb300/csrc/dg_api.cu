@@ -420,7 +420,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
     return fail(DG_ERR_INVALID_ARG, "the fused SwiGLU form is masked, with FP32 scales");
   if (swiglu && N % 256 != 0)
     return fail(DG_ERR_ALIGNMENT, "fused SwiGLU: B must hold 2I rows per group with I a multiple of 128");
-  if ((a_mn || b_mn) && (mode != dg::kDense || block_scaled))
+  if ((a_mn || b_mn) && mode != dg::kDense)
     return fail(DG_ERR_INVALID_ARG, "the NN/TN/TT layouts are dense, with FP32 scales");
   if (rows == 0 || N == 0 || G == 0) return DG_OK;
   if (K == 0) return fail(DG_ERR_INVALID_ARG, "K must be positive");
@@ -807,6 +807,42 @@ dg_status dg_fp8_gemm_tt(const uint8_t* A, const float* sA, const uint8_t* B, co
 dg_status dg_fp8_gemm_tt_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, float* D, int M,
                              int N, int K, dg_stream_t stream) {
   return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), false,
+                  nullptr, false, false, true, false);
+}
+
+dg_status dg_fp8_gemm_nn_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB, uint16_t* D,
+                               int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true,
+                  nullptr, false, false, false, true);
+}
+
+dg_status dg_fp8_gemm_nn_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB, float* D,
+                                   int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true,
+                  nullptr, false, false, false, true);
+}
+
+dg_status dg_fp8_gemm_tn_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB, uint16_t* D,
+                               int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true,
+                  nullptr, false, false, true, true);
+}
+
+dg_status dg_fp8_gemm_tn_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB, float* D,
+                                   int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true,
+                  nullptr, false, false, true, true);
+}
+
+dg_status dg_fp8_gemm_tt_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB, uint16_t* D,
+                               int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, false, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true,
+                  nullptr, false, false, true, false);
+}
+
+dg_status dg_fp8_gemm_tt_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB, float* D,
+                                   int M, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kDense, true, A, sA, B, sB, nullptr, D, M, N, K, 1, static_cast<cudaStream_t>(stream), true,
                   nullptr, false, false, true, false);
 }
 

@@ -187,8 +187,16 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
             if (!ok) break;
             uint8_t* sa = smem + s * Plan::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
-            tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
-            tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
+            if (p.flags & kFlagAMN)   // A stored [K, M]: the box is 128 K-rows x 128 M-bytes
+              tma_load_2d(&tmA, sa, &full_bar[s], tile.a_row, kb * 128, policy);
+            else
+              tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
+            if (p.flags & kFlagBMN) {  // B stored [K, N]: two boxes of 128 K-rows x 128 N-bytes, 16 KB apart
+              tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], b_row, kb * 128, policy);
+              tma_load_2d(&tmB, sa + Plan::kABytes + 128 * 128, &full_bar[s], b_row + 128, kb * 128, policy);
+            } else {
+              tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, b_row, policy);
+            }
             issued_phase[s] = (int)ph;
           }
         }
@@ -209,6 +217,11 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       // ---------------------------------------------------------------- block-scaled MMA issuer
       uint32_t it = 0, sf_it = 0, tile_it = 0;
       bool alive = true, issued_any = false;
+      // An operand stored MN-major (the NN/TN/TT layouts) is read with an MN-major descriptor: one
+      // K=32 step is +32 rows of 128 bytes (+256 in the >>4 address field) instead of +32 bytes.
+      const bool a_mn = (p.flags & kFlagAMN) != 0, b_mn = (p.flags & kFlagBMN) != 0;
+      const uint32_t a_step = a_mn ? 256u : 2u, b_step = b_mn ? 256u : 2u;
+      const uint32_t idesc_layout = kIdesc | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
       for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
         const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
@@ -233,15 +246,16 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_addr = smem_u32(smem + s * Plan::kStageBytes);
-            const uint64_t adesc = make_sw128_kmajor_desc(a_addr);
-            const uint64_t bdesc = make_sw128_kmajor_desc(a_addr + Plan::kABytes);
-            const uint32_t idesc = idesc_with_sf_id(kIdesc, (uint32_t)(kb & 3));
+            const uint64_t adesc = a_mn ? make_sw128_mnmajor_desc(a_addr, 128 * 128) : make_sw128_kmajor_desc(a_addr);
+            const uint64_t bdesc = b_mn ? make_sw128_mnmajor_desc(a_addr + Plan::kABytes, 128 * 128)
+                                        : make_sw128_kmajor_desc(a_addr + Plan::kABytes);
+            const uint32_t idesc = idesc_with_sf_id(idesc_layout, (uint32_t)(kb & 3));
             const uint32_t sfa = tmem_base + kSfCol0 + slot * kSfSlotCols;
             const uint32_t sfb = sfa + kSfbOff;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field
-              mma_e4m3_block_scaled(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc, sfa, sfb,
+              // K-major: +32 bytes along K inside the 128-byte swizzled row (+2 in the >>4 field)
+              mma_e4m3_block_scaled(tmem_base, adesc + a_step * k, bdesc + b_step * k, idesc, sfa, sfb,
                                     (kb > tile.kb0 || k > 0) ? 1u : 0u);
             }
             issued_any = true;

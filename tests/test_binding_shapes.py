@@ -144,6 +144,21 @@ def test_layout_shapes(layout):
     _refused(fn, args, 5, M + 16)                          # sizes that disagree with the tensors
 
 
+@pytest.mark.parametrize("layout", ["nn", "tn", "tt"])
+def test_layout_ue8m0_shapes(layout):
+    a_t, b_n = {"nn": (False, True), "tn": (True, True), "tt": (True, False)}[layout]
+    fn = getattr(dg, f"dg_fp8_gemm_{layout}_ue8m0")
+    nkq = cdiv(NKB, 4)
+    A = u8(K, M) if a_t else u8(M, K)
+    B = u8(K, N) if b_n else u8(N, K)
+    args = [A, i32(nkq, a4(M)), B, i32(NNB, nkq), bf16(M, N), M, N, K]
+    _accepted(fn, args)
+    _refused(fn, args, 1, i32(NKB, a4(M)))                 # FP32-scale layout to the packed call
+    _refused(fn, args, 3, i32(NNB, NKB))
+    _refused(fn, args, 0, u8(M, K) if a_t else u8(K, M))
+    _accepted(getattr(dg, f"dg_fp8_gemm_{layout}_ue8m0_f32"), args[:4] + [f32(M, N), M, N, K])
+
+
 def test_k_grouped_shapes():
     KT, MG, NG = 1024, 256, 384
     args = [u8(KT, MG), f32(KT // 128, a4(MG)), u8(KT, NG), f32(cdiv(NG, 128), KT // 128), i32(G + 1), bf16(G, MG, NG)]
