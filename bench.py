@@ -814,20 +814,23 @@ def run_all_configs(args):
                dict(scales, cfg=query_config(dg, 2, M_max, N, K, G)))
     for (M, N, K) in ((4096, 2112, 7168), (4096, 576, 7168), (4096, 7168, 32768)) if want(5) else ():
         dense("5 stress (Student-t, outliers)", M, N, K, dist=dg_inputs.STUDENT_T3, outliers=0.01)
-    # the masked form fused with SwiGLU (FP32 scales only): B holds 2I rows, H has I columns
-    if not UE8M0 and want(7):
+    # the masked form fused with SwiGLU (both scale forms): B holds 2I rows, H has I columns
+    if want(7):
         for (N2, K) in ((4096, 7168),):
             G, M_max, I = 16, 256, N2 // 2
             mm = dg_inputs.make_masked_m(G, M_max, seed=0)
-            a = dg_inputs.make_masked_a(G, M_max, K, seed=0)
-            b = dg_inputs.make_b(G, N2, K, seed=0)
-            A, sA, B, sB, MM = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(mm)
+            a = dg_inputs.make_masked_a(G, M_max, K, seed=0, ue8m0=UE8M0)
+            b = dg_inputs.make_b(G, N2, K, seed=0, ue8m0=UE8M0)
+            gsA, gsB = gpu_scales(a, b)
+            A, sA, B, sB, MM = dev(a.A), dev(gsA), dev(b.B), dev(gsB), dev(mm)
             H = torch.empty(G, M_max, I, dtype=torch.bfloat16, device="cuda")
-            ms = timeit(lambda: dg.dg_fp8_grouped_masked_swiglu(A, sA, B, sB, MM, H))
+            fn = dg.dg_fp8_grouped_masked_swiglu_ue8m0 if UE8M0 else dg.dg_fp8_grouped_masked_swiglu
+            ms = timeit(lambda: fn(A, sA, B, sB, MM, H))
             valid = int(mm.sum())
             nkb = -(-K // 128)
+            nks = -(-nkb // 4) if UE8M0 else nkb
             active = int((mm > 0).sum())
-            nbytes = valid * K + active * N2 * K + 4 * valid * nkb + 4 * G * (N2 // 128) * nkb + 2 * valid * I
+            nbytes = valid * K + active * N2 * K + 4 * valid * nks + 4 * G * (N2 // 128) * nks + 2 * valid * I
             report("7 masked + SwiGLU (fused)", f"G=16 M_max=256 sum(masked_m)={valid} 2I={N2} K={K}",
                    2.0 * valid * N2 * K, nbytes, ms, dict(scales))
             del A, B, H

@@ -252,6 +252,17 @@ dg_status dg_fp8_grouped_masked_swiglu(const uint8_t* A, const float* sA, const 
 dg_status dg_fp8_grouped_masked_swiglu_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                                            const int32_t* masked_m, float* H, int G, int M_max, int N, int K,
                                            dg_stream_t stream);
+/* The fused SwiGLU with power-of-two scales packed as UE8M0, on the block-scaled kernel: the layouts
+   of A, B, masked_m and H as for dg_fp8_grouped_masked_swiglu, the packed scale layouts of
+   dg_fp8_grouped_masked_ue8m0 (sA [G][ceil(ceil(K/128)/4)][align4(M_max)], sB [G][N/128][ceil(ceil(K/128)/4)],
+   N = 2I). The accumulator of a tile stays in tensor memory for the whole K loop, so each epilogue
+   warp reads both its gate and its up columns from it; silu as in the FP32-scale form. */
+dg_status dg_fp8_grouped_masked_swiglu_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                             const int32_t* sB, const int32_t* masked_m, uint16_t* H, int G,
+                                             int M_max, int N, int K, dg_stream_t stream);
+dg_status dg_fp8_grouped_masked_swiglu_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                                 const int32_t* sB, const int32_t* masked_m, float* H, int G,
+                                                 int M_max, int N, int K, dg_stream_t stream);
 
 /*
  * Accumulating dense GEMM: D = C + A·Bᵀ, the full definition of fp8_gemm_nt ("DeepGEMM: İnce

@@ -40,7 +40,8 @@ __all__ = [
     "dg_set_tail_splits", "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
-    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
+    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_ue8m0",
+    "dg_fp8_grouped_masked_swiglu_ue8m0_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
     "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32",
     "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
@@ -61,7 +62,8 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
-    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
+    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_ue8m0",
+    "dg_fp8_grouped_masked_swiglu_ue8m0_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
     "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32",
     "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32",
@@ -100,7 +102,8 @@ def load(build_if_missing: bool = True):
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
     for name in ("dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_fp8_grouped_masked_ue8m0",
                  "dg_fp8_grouped_masked_ue8m0_f32", "dg_fp8_grouped_masked_swiglu",
-                 "dg_fp8_grouped_masked_swiglu_f32"):
+                 "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_ue8m0",
+                 "dg_fp8_grouped_masked_swiglu_ue8m0_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
     lib.dg_get_tma_aligned_size.restype, lib.dg_get_tma_aligned_size.argtypes = i32, [i32, i32]
@@ -452,6 +455,15 @@ def dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H, stream=None):
 
 def dg_fp8_grouped_masked_swiglu_f32(A, sA, B, sB, masked_m, H, stream=None):
     return _masked("dg_fp8_grouped_masked_swiglu_f32", True, A, sA, B, sB, masked_m, H, stream)
+
+
+def dg_fp8_grouped_masked_swiglu_ue8m0(A, sA, B, sB, masked_m, H, stream=None):
+    """The fused SwiGLU with packed UE8M0 scales (int32 words, four K-groups each)."""
+    return _masked("dg_fp8_grouped_masked_swiglu_ue8m0", False, A, sA, B, sB, masked_m, H, stream)
+
+
+def dg_fp8_grouped_masked_swiglu_ue8m0_f32(A, sA, B, sB, masked_m, H, stream=None):
+    return _masked("dg_fp8_grouped_masked_swiglu_ue8m0_f32", True, A, sA, B, sB, masked_m, H, stream)
 
 
 def dg_fp8_gemm_nt_ue8m0(A, sA, B, sB, D, stream=None):

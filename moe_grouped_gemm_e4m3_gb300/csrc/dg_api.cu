@@ -416,7 +416,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   }
   if (accumulate && (!C || !out_f32 || mode != dg::kDense))
     return fail(DG_ERR_INVALID_ARG, "the accumulating form needs a C pointer and FP32 D (dense only)");
-  if (swiglu && (mode != dg::kMasked || block_scaled || accumulate))
+  if (swiglu && (mode != dg::kMasked || accumulate))
     return fail(DG_ERR_INVALID_ARG, "the fused SwiGLU form is masked, with FP32 scales");
   if (swiglu && N % 256 != 0)
     return fail(DG_ERR_ALIGNMENT, "fused SwiGLU: B must hold 2I rows per group with I a multiple of 128");
@@ -458,7 +458,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   if (swiglu) {
     // one tile = 128 gate rows + 128 up rows of B; no split-K
     cfg.block_n = 256;
-    cfg.stages = dg::stages_for(256);
+    cfg.stages = block_scaled ? dg::BsSmemPlan::kStages : dg::stages_for(256);
     cfg.splits = 1;
     cfg.kb_per_split = ceil_div(K, 128);
     cfg.tiles = ceil_div(rows, 128) * G * (d_cols / 128);
@@ -587,7 +587,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   }
   cudaError_t e;
   if (swiglu) {
-    e = dg::launch_masked_swiglu(a);
+    e = block_scaled ? dg::launch_bs_swiglu(a) : dg::launch_masked_swiglu(a);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return DG_OK;
   }
@@ -858,6 +858,20 @@ dg_status dg_fp8_grouped_masked_swiglu_f32(const uint8_t* A, const float* sA, co
                                            dg_stream_t stream) {
   return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, H, M_max, N, K, G, static_cast<cudaStream_t>(stream),
                   false, nullptr, false, true);
+}
+
+dg_status dg_fp8_grouped_masked_swiglu_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,
+                                             const int32_t* masked_m, uint16_t* H, int G, int M_max, int N, int K,
+                                             dg_stream_t stream) {
+  return run_gemm(dg::kMasked, false, A, sA, B, sB, masked_m, H, M_max, N, K, G, static_cast<cudaStream_t>(stream),
+                  true, nullptr, false, true);
+}
+
+dg_status dg_fp8_grouped_masked_swiglu_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                                 const int32_t* sB, const int32_t* masked_m, float* H, int G,
+                                                 int M_max, int N, int K, dg_stream_t stream) {
+  return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, H, M_max, N, K, G, static_cast<cudaStream_t>(stream),
+                  true, nullptr, false, true);
 }
 
 dg_status dg_fp8_gemm_nt_acc_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, const float* C,

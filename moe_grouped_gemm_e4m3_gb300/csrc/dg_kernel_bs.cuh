@@ -82,7 +82,11 @@ constexpr uint32_t kSfSlotCols = 32;
 constexpr uint32_t kSfbOff = 16;
 static_assert(kSfCol0 + BsSmemPlan::kSfSlots * kSfSlotCols <= kBsTmemCols, "scale slots exceed TMEM");
 
-template <Mode MODE, bool OUT_F32>
+// SWIGLU (masked form only): the tile's 256 B rows are 128 gate rows (block n of [0, I)) and the
+// matching 128 up rows (block n of [I, 2I)), and the epilogue stores H = silu(gate)·up, 128
+// columns of H per tile. The whole K loop accumulates in TMEM, so each epilogue warp loads both
+// its gate and its up columns itself: no hand-over between warps.
+template <Mode MODE, bool OUT_F32, bool SWIGLU = false>
 __global__ void __launch_bounds__(BsRoles::kThreads, 1)
     fp8_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
@@ -94,6 +98,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
   constexpr int SLOTS = Plan::kSfSlots;
   // cluster split-K (kFlagClusterSplit) is compiled into the dense and contiguous forms only
   constexpr bool kClusterCapable = MODE == kDense || MODE == kContiguous;
+  static_assert(!SWIGLU || MODE == kMasked, "fused SwiGLU: masked form only");
   constexpr uint32_t kIdesc = make_idesc_e4m3_bs(128, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -191,7 +196,12 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
               tma_load_2d(&tmA, sa, &full_bar[s], tile.a_row, kb * 128, policy);
             else
               tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
-            if (p.flags & kFlagBMN) {  // B stored [K, N]: two boxes of 128 K-rows x 128 N-bytes, 16 KB apart
+            if constexpr (SWIGLU) {
+              // gate rows 128·n .. and up rows I + 128·n .. (B's tensor map box is 128 rows)
+              const int gate_row = tile.g * p.N + tile.n_blk * 128;
+              tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], kb * 128, gate_row, policy);
+              tma_load_2d(&tmB, sa + Plan::kABytes + 128 * 128, &full_bar[s], kb * 128, gate_row + p.swiglu_i, policy);
+            } else if (p.flags & kFlagBMN) {  // B stored [K, N]: two boxes of 128 K-rows x 128 N-bytes, 16 KB apart
               tma_load_2d(&tmB, sa + Plan::kABytes, &full_bar[s], b_row, kb * 128, policy);
               tma_load_2d(&tmB, sa + Plan::kABytes + 128 * 128, &full_bar[s], b_row + 128, kb * 128, policy);
             } else {
@@ -312,14 +322,17 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         const bool row_exists = row_in_tile < tile.rows;
         const int m_local = tile.m_blk * 128 + row_in_tile;
         const uint32_t* sfa_ptr = reinterpret_cast<const uint32_t*>(p.sA) + (MODE == kMasked ? (size_t)tile.g * nkq * p.ldsa : 0) + m_local;
-        const int nb0 = tile.n_blk * 2;        // the tile's two 128-row scale blocks of B
+        // the tile's two 128-row scale blocks of B: 2n and 2n + 1, or (SwiGLU) gate block n and up
+        // block I/128 + n
+        const int nb0 = SWIGLU ? tile.n_blk : tile.n_blk * 2;
         const uint32_t* sfb_ptr = reinterpret_cast<const uint32_t*>(p.sB) + ((size_t)tile.g * p.nnb + nb0) * nkq;
-        const bool has_nb1 = nb0 + 1 < p.nnb;
+        const uint32_t* sfb1_ptr = SWIGLU ? sfb_ptr + (size_t)(p.swiglu_i / 128) * nkq : sfb_ptr + nkq;
+        const bool has_nb1 = SWIGLU || nb0 + 1 < p.nnb;
         const int q_end = (tile.kb1 - 1) >> 2;
         for (int quad = tile.kb0 >> 2; quad <= q_end; ++quad, ++sf_it) {
           const uint32_t a = row_exists ? __ldg(sfa_ptr + (size_t)quad * p.ldsa) : 0x7F7F7F7Fu;
           const uint32_t b0 = __ldg(sfb_ptr + quad);
-          const uint32_t b1 = has_nb1 ? __ldg(sfb_ptr + nkq + quad) : 0x7F7F7F7Fu;
+          const uint32_t b1 = has_nb1 ? __ldg(sfb1_ptr + quad) : 0x7F7F7F7Fu;
           const uint32_t slot = sf_it % SLOTS;
           if (!mbar_wait(&sf_empty_bar[slot], ((sf_it / SLOTS) & 1) ^ 1, abort_flag, p.status, p.flags)) {
             alive = false;
@@ -385,7 +398,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&desc_empty_bar[ds]);
         if (end) break;
-        active = (n_blk0 * BN + cgrp * EPI_COLS < p.N) && __any_sync(0xffffffffu, row_in_tile < rows0);
+        active = (SWIGLU || n_blk0 * BN + cgrp * EPI_COLS < p.N) && __any_sync(0xffffffffu, row_in_tile < rows0);
       }
       // this warp's 32x128 block of the accumulator (live only within one tile)
       uint32_t accu[EPI_COLS];
@@ -395,13 +408,16 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       ++tile_it;
       tc_fence_after();
       if (active) {
-        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cgrp * EPI_COLS);
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
 #pragma unroll
         for (int c = 0; c < EPI_COLS / 32; c += 2) {
           uint32_t(&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&accu[c * 32]);
           uint32_t(&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&accu[(c + 1) * 32]);
-          tmem_ld_32x32b_x32(taddr + c * 32, r0);
-          tmem_ld_32x32b_x32(taddr + (c + 1) * 32, r1);
+          // SwiGLU: registers 0..63 take gate columns 64·cgrp.., registers 64..127 the matching up
+          // columns 128 + 64·cgrp..; otherwise the warp's 128 columns in order
+          const uint32_t col = SWIGLU ? (uint32_t)((c == 0 ? 0 : 128) + cgrp * 64) : (uint32_t)(cgrp * EPI_COLS + c * 32);
+          tmem_ld_32x32b_x32(lane_addr + col, r0);
+          tmem_ld_32x32b_x32(lane_addr + col + 32, r1);
           tmem_ld_wait(r0);
           reg_fence(r1);
         }
@@ -418,6 +434,66 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       const bool row_exists = row_in_tile < tile.rows;
       const int n_col0 = tile.n_blk * BN + cgrp * EPI_COLS;
       const bool col_exists = n_col0 < p.N;
+
+      if constexpr (SWIGLU) {
+        // H = silu(gate)·up for this warp's 64 of the tile's 128 columns of H (row stride I)
+        if (!active || !__any_sync(0xffffffffu, row_exists)) continue;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = silu_f32(acc[j]) * acc[64 + j];
+        const int h_col0 = tile.n_blk * 128 + cgrp * 64;
+        if (__all_sync(0xffffffffu, row_exists)) {
+          constexpr int kColsPerBox = OUT_F32 ? 16 : 32;
+#pragma unroll
+          for (int chunk = 0; chunk < 64 / kColsPerBox; ++chunk) {
+            const uint32_t sel = store_count & 1;
+            if (store_count >= 2) {
+              if (lane == 0) tma_store_wait_read_1();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t w0, w1, w2, w3;
+              if constexpr (OUT_F32) {
+                const int c = chunk * 16 + j * 4;
+                w0 = accu[c]; w1 = accu[c + 1]; w2 = accu[c + 2]; w3 = accu[c + 3];
+              } else {
+                const int c = chunk * 32 + j * 8;
+                w0 = pack_bf16x2(acc[c], acc[c + 1]); w1 = pack_bf16x2(acc[c + 2], acc[c + 3]);
+                w2 = pack_bf16x2(acc[c + 4], acc[c + 5]); w3 = pack_bf16x2(acc[c + 6], acc[c + 7]);
+              }
+              const uint32_t phys = (uint32_t)(j ^ ((lane >> 1) & 3));
+              st_shared_v4(staging_addr + sel * Plan::kStagingBox + lane * 64 + phys * 16, w0, w1, w2, w3);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, staging + sel * Plan::kStagingBox, h_col0 + chunk * kColsPerBox, tile.a_row + quad * 32);
+              tma_store_commit();
+            }
+            ++store_count;
+            __syncwarp();
+          }
+        } else if (row_exists) {
+          // predicated plain stores: rows past masked_m stay untouched
+          const size_t hrow = (size_t)(tile.a_row + row_in_tile) * p.swiglu_i + h_col0;
+          if constexpr (OUT_F32) {
+            float* dst = reinterpret_cast<float*>(p.D) + hrow;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4)
+              *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+          } else {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + hrow;
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(acc[j], acc[j + 1]); v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+              v.z = pack_bf16x2(acc[j + 4], acc[j + 5]); v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+              *reinterpret_cast<uint4*>(dst + j) = v;
+            }
+          }
+        }
+        continue;
+      }
 
       if (kClusterCapable && (p.flags & kFlagClusterSplit)) {
         // one unit per CTA: the partial goes to this CTA's stage buffers (idle once the MMA is

@@ -39,6 +39,8 @@ cudaError_t launch_kgrouped(const LaunchArgs& a);
 cudaError_t launch_masked_swiglu(const LaunchArgs& a);
 // The block-scaled kernel for packed UE8M0 scales (block_n is always 256).
 cudaError_t launch_bs(const LaunchArgs& a, Mode mode);
+// The block-scaled masked form fused with SwiGLU.
+cudaError_t launch_bs_swiglu(const LaunchArgs& a);
 // How many clusters of `cluster` CTAs of the dense / contiguous instantiation for (block_n,
 // out_f32) can be resident at once (0 if the query fails).
 int cluster_capacity_dense(int block_n, bool out_f32, int cluster);
@@ -133,9 +135,9 @@ int cluster_capacity_mode(int block_n, bool out_f32, int cluster) {
   return out_f32 ? cluster_capacity_instance<128, MODE, true>(cluster) : cluster_capacity_instance<128, MODE, false>(cluster);
 }
 
-template <Mode MODE, bool OUT_F32>
+template <Mode MODE, bool OUT_F32, bool SWIGLU = false>
 cudaError_t launch_bs_instance(const LaunchArgs& a) {
-  auto kernel = fp8_gemm_bs_kernel<MODE, OUT_F32>;
+  auto kernel = fp8_gemm_bs_kernel<MODE, OUT_F32, SWIGLU>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

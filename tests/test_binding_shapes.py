@@ -126,6 +126,12 @@ def test_swiglu_shapes():
     _accepted(fn, args)
     _refused(fn, args, 5, bf16(G, MM, N2))              # H is I = N2/2 wide
     _refused(fn, args, 3, f32(G, N2 // 256, NKB))
+    nkq = cdiv(NKB, 4)
+    pargs = [u8(G, MM, K), i32(G, nkq, a4(MM)), u8(G, N2, K), i32(G, N2 // 128, nkq), i32(G), bf16(G, MM, N2 // 2)]
+    _accepted(dg.dg_fp8_grouped_masked_swiglu_ue8m0, pargs)
+    _accepted(dg.dg_fp8_grouped_masked_swiglu_ue8m0_f32, pargs[:5] + [f32(G, MM, N2 // 2)])
+    _refused(dg.dg_fp8_grouped_masked_swiglu_ue8m0, pargs, 1, i32(G, NKB, a4(MM)))
+    _refused(dg.dg_fp8_grouped_masked_swiglu_ue8m0, pargs, 5, bf16(G, MM, N2))
 
 
 @pytest.mark.parametrize("layout", ["nn", "tn", "tt"])

@@ -1,4 +1,5 @@
-"""GPU parity of the masked grouped GEMM fused with SwiGLU against the CPU oracle.
+"""GPU parity of the masked grouped GEMM fused with SwiGLU against the CPU oracle, with FP32 scales
+(the FP32-scale kernel) and with power-of-two scales packed as UE8M0 (the block-scaled kernel).
 
 H[g,m,j] = silu(D[g,m,j]) · D[g,m,I+j] over the valid rows m < masked_m[g] (B holds the I gate rows,
 then the I up rows, of each group). Checked: rows past masked_m untouched (sentinel bits), the BF16
@@ -25,14 +26,23 @@ def dg():
     assert m.dg_get_device_status() == 0
 
 
-def _run(dg, a, b, masked_m):
+SCALES = ["fp32", "ue8m0"]
+
+
+def _run(dg, a, b, masked_m, scales="fp32"):
     G, M_max, _ = a.A.shape
     I = b.B.shape[1] // 2
-    A, sA, B, sB, MM = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(masked_m)
+    A, B, MM = dev(a.A), dev(b.B), dev(masked_m)
     H = bf16_sentinel((G, M_max, I))
     H32 = f32_sentinel((G, M_max, I))
-    dg.dg_fp8_grouped_masked_swiglu(A, sA, B, sB, MM, H)
-    dg.dg_fp8_grouped_masked_swiglu_f32(A, sA, B, sB, MM, H32)
+    if scales == "ue8m0":
+        sA, sB = dev(dg_inputs.pack_ue8m0_a(a.sA)), dev(dg_inputs.pack_ue8m0_b(b.sB))
+        dg.dg_fp8_grouped_masked_swiglu_ue8m0(A, sA, B, sB, MM, H)
+        dg.dg_fp8_grouped_masked_swiglu_ue8m0_f32(A, sA, B, sB, MM, H32)
+    else:
+        sA, sB = dev(a.sA), dev(b.sB)
+        dg.dg_fp8_grouped_masked_swiglu(A, sA, B, sB, MM, H)
+        dg.dg_fp8_grouped_masked_swiglu_f32(A, sA, B, sB, MM, H32)
     torch.cuda.synchronize()
     return H, H32
 
@@ -41,13 +51,15 @@ def _valid(masked_m, M_max):
     return np.arange(M_max)[None, :] < np.clip(masked_m, 0, M_max)[:, None]
 
 
-@pytest.mark.parametrize("I,K", [(128, 384), (256, 1024), (384, 256)])
-def test_swiglu_full_parity(dg, I, K):
+@pytest.mark.parametrize("scales", SCALES)
+@pytest.mark.parametrize("I,K", [(128, 384), (256, 1024), (384, 256), (256, 640)])
+def test_swiglu_full_parity(dg, I, K, scales):
     masked_m = np.array([0, 1, 127, 128, 129, 256], np.int32)
     G, M_max = len(masked_m), 256
-    a = dg_inputs.make_masked_a(G, M_max, K, seed=41)
-    b = dg_inputs.make_b(G, 2 * I, K, seed=41)
-    H, H32 = _run(dg, a, b, masked_m)
+    ue = scales == "ue8m0"
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=41, ue8m0=ue)
+    b = dg_inputs.make_b(G, 2 * I, K, seed=41, ue8m0=ue)
+    H, H32 = _run(dg, a, b, masked_m, scales)
     ref, _, bad = oracle.grouped_masked_swiglu(a.A, a.sA, b.B, b.sB, masked_m)
     assert bad == 0
     valid = torch.from_numpy(_valid(masked_m, M_max))
@@ -56,15 +68,17 @@ def test_swiglu_full_parity(dg, I, K):
     assert torch.all(torch.isnan(H32.cpu()[~valid]))
     assert torch.equal(hb[valid], rne_bf16_bits(H32)[valid])
     v = valid.numpy()
-    assert_accurate(H32.cpu().numpy()[v], hb.numpy()[v], ref[v], f"swiglu I={I} K={K}")
+    assert_accurate(H32.cpu().numpy()[v], hb.numpy()[v], ref[v], f"swiglu/{scales} I={I} K={K}")
 
 
-def test_swiglu_decode_sampled(dg):
+@pytest.mark.parametrize("scales", SCALES)
+def test_swiglu_decode_sampled(dg, scales):
     G, M_max, I, K = 16, 256, 2048, 7168
+    ue = scales == "ue8m0"
     masked_m = dg_inputs.make_masked_m(G, M_max, seed=0)
-    a = dg_inputs.make_masked_a(G, M_max, K, seed=0)
-    b = dg_inputs.make_b(G, 2 * I, K, seed=0)
-    H, H32 = _run(dg, a, b, masked_m)
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=0, ue8m0=ue)
+    b = dg_inputs.make_b(G, 2 * I, K, seed=0, ue8m0=ue)
+    H, H32 = _run(dg, a, b, masked_m, scales)
     valid = _valid(masked_m, M_max)
     vt = torch.from_numpy(valid)
     hb = bits16(H).cpu()
@@ -76,7 +90,7 @@ def test_swiglu_decode_sampled(dg):
     gs, ms = gs[pick], ms[pick]
     js = rng.integers(0, I, len(gs))
     ref = oracle.masked_swiglu_sampled(a.A, a.sA, b.B, b.sB, gs, ms, js)
-    assert_accurate(H32.cpu().numpy()[gs, ms, js], hb.numpy()[gs, ms, js], ref, "swiglu decode")
+    assert_accurate(H32.cpu().numpy()[gs, ms, js], hb.numpy()[gs, ms, js], ref, f"swiglu/{scales} decode")
 
 
 def test_swiglu_rejects_bad_width(dg):
