@@ -851,19 +851,22 @@ def run_all_configs(args):
                    dict(scales, cfg=query_config(dg, 0, M, N, K)))
             del A, B, D
     # the K-grouped form (weight gradients): 4 experts with 1024, 0, 2048 and 512 tokens
-    if not UE8M0 and want(9):
+    if want(9):
         M, N = 2048, 7168
         off = np.array([0, 1024, 1024, 3072, 3584], np.int32)
         K = int(off[-1])
-        a = dg_inputs.make_a(M, K, seed=0)
-        b = dg_inputs.make_b(1, N, K, seed=0)
+        a = dg_inputs.make_a(M, K, seed=0, ue8m0=UE8M0)
+        b = dg_inputs.make_b(1, N, K, seed=0, ue8m0=UE8M0)
+        gsA, gsB = gpu_scales(a, b)
         A, B = dev(np.ascontiguousarray(a.A.T)), dev(np.ascontiguousarray(b.B[0].T))
-        sA, sB, O = dev(a.sA), dev(b.sB[0]), dev(off)
+        sA, sB, O = dev(gsA), dev(gsB[0]), dev(off)
         G = len(off) - 1
         D = torch.empty(G, M, N, dtype=torch.bfloat16, device="cuda")
-        ms = timeit(lambda: dg.dg_fp8_k_grouped_gemm_tn_contiguous(A, sA, B, sB, O, D))
+        fn = dg.dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0 if UE8M0 else dg.dg_fp8_k_grouped_gemm_tn_contiguous
+        ms = timeit(lambda: fn(A, sA, B, sB, O, D))
         nkb, nnb = K // 128, -(-N // 128)
-        nbytes = M * K + N * K + 4 * M * nkb + 4 * nnb * nkb + 2 * G * M * N
+        nks = -(-nkb // 4) if UE8M0 else nkb
+        nbytes = M * K + N * K + 4 * M * nks + 4 * nnb * nks + 2 * G * M * N
         report("9 K-grouped (weight gradient)", f"G=4 M={M} N={N} K_total={K} (1024,0,2048,512)", 2.0 * M * N * K,
                nbytes, ms, dict(scales))
         del A, B, D

@@ -230,6 +230,17 @@ dg_status dg_fp8_k_grouped_gemm_tn_contiguous(const uint8_t* A, const float* sA,
 dg_status dg_fp8_k_grouped_gemm_tn_contiguous_f32(const uint8_t* A, const float* sA, const uint8_t* B,
                                                   const float* sB, const int32_t* k_offsets, float* D, int G, int M,
                                                   int N, int K_total, dg_stream_t stream);
+/* The K-grouped form with power-of-two scales packed as UE8M0, on the block-scaled kernel: A, B,
+   k_offsets and D as above; sA [ceil(K_total/512)][align4(M)] and sB [ceil(N/128)][ceil(K_total/512)]
+   int32, four 128-deep K-blocks per word along the whole K_total axis (a group whose offset is not a
+   multiple of 512 starts inside a word; the kernel picks each K-block's byte). An empty group stores
+   zeros. */
+dg_status dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                                    const int32_t* sB, const int32_t* k_offsets, uint16_t* D, int G,
+                                                    int M, int N, int K_total, dg_stream_t stream);
+dg_status dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                                        const int32_t* sB, const int32_t* k_offsets, float* D, int G,
+                                                        int M, int N, int K_total, dg_stream_t stream);
 
 /*
  * Masked grouped GEMM fused with SwiGLU (MoE decode): the up/gate projection of each expert and the

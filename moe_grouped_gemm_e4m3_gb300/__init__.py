@@ -44,7 +44,8 @@ __all__ = [
     "dg_fp8_grouped_masked_swiglu_ue8m0_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
     "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32",
-    "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
+    "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32",
+    "dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0", "dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
     "DG_DEV_TIMEOUT",
 ]
@@ -67,6 +68,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
     "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32",
     "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32",
+    "dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0", "dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32",
 )
 
 
@@ -120,7 +122,8 @@ def load(build_if_missing: bool = True):
     for name in ("dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, P]
-    for name in ("dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32"):
+    for name in ("dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32",
+                 "dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0", "dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
     for name in ("dg_query_config", "dg_query_config_ue8m0"):
@@ -427,12 +430,14 @@ def _k_grouped(name, f32, A, sA, B, sB, k_offsets, D, stream):
     G = o[0] - 1
     if b[0] != K_total:
         raise ValueError(f"B has K_total = {b[0]}, A has K_total = {K_total}")
-    _expect(sA, "sA", (_cdiv(K_total, 128), _align4(M)))
-    _expect(sB, "sB", (_cdiv(N, 128), _cdiv(K_total, 128)))
+    nks = _scale_k(name, K_total)
+    _expect(sA, "sA", (nks, _align4(M)))
+    _expect(sB, "sB", (_cdiv(N, 128), nks))
     _expect(D, "D", (G, M, N))
     lib = load()
-    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()),
-                              _ptr(sB, "sB", _f32()), _ptr(k_offsets, "k_offsets", (torch.int32,)),
+    st = _scale_types(name)
+    _check(getattr(lib, name)(_ptr(A, "A", _fp8_types()), _ptr(sA, "sA", st), _ptr(B, "B", _fp8_types()),
+                              _ptr(sB, "sB", st), _ptr(k_offsets, "k_offsets", (torch.int32,)),
                               _ptr(D, "D", _d_types(f32)), G, M, N, K_total, _stream(stream)))
     return D
 
@@ -445,6 +450,16 @@ def dg_fp8_k_grouped_gemm_tn_contiguous(A, sA, B, sB, k_offsets, D, stream=None)
 
 def dg_fp8_k_grouped_gemm_tn_contiguous_f32(A, sA, B, sB, k_offsets, D, stream=None):
     return _k_grouped("dg_fp8_k_grouped_gemm_tn_contiguous_f32", True, A, sA, B, sB, k_offsets, D, stream)
+
+
+def dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0(A, sA, B, sB, k_offsets, D, stream=None):
+    """The K-grouped GEMM with packed UE8M0 scales: sA [ceil(K_total/512), align4(M)], sB
+    [ceil(N/128), ceil(K_total/512)] int32 (four K-blocks per word along K_total)."""
+    return _k_grouped("dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0", False, A, sA, B, sB, k_offsets, D, stream)
+
+
+def dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32(A, sA, B, sB, k_offsets, D, stream=None):
+    return _k_grouped("dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32", True, A, sA, B, sB, k_offsets, D, stream)
 
 
 def dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H, stream=None):

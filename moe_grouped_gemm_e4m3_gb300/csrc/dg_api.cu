@@ -607,8 +607,11 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
 
 // The K-grouped GEMM: A stored [K_total, M], B stored [K_total, N] (both MN-major), D [G, M, N];
 // group g sums the K-blocks [offsets[g], offsets[g+1]) / 128 (offsets on the device).
-dg_status run_k_grouped(bool out_f32, const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
-                        const int32_t* offsets, void* D, int G, int M, int N, int K_total, cudaStream_t stream) {
+// block_scaled: sA/sB are packed UE8M0 words (sA [ceil(nkb/4)][ldsa], sB [ceil(N/128)][ceil(nkb/4)],
+// nkb = K_total/128), run on the block-scaled kernel (BN = 256).
+dg_status run_k_grouped(bool out_f32, const uint8_t* A, const void* sA, const uint8_t* B, const void* sB,
+                        const int32_t* offsets, void* D, int G, int M, int N, int K_total, cudaStream_t stream,
+                        bool block_scaled = false) {
   t_last_error.clear();
   if (G < 0 || M < 0 || N < 0 || K_total < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
   if (G == 0 || M == 0 || N == 0) return DG_OK;
@@ -630,7 +633,7 @@ dg_status run_k_grouped(bool out_f32, const uint8_t* A, const float* sA, const u
   dg_status s = device_state(&st);
   if (s != DG_OK) return s;
   const int sms = effective_sms(*st);
-  const int bn = N > 128 ? 256 : 128;
+  const int bn = (block_scaled || N > 128) ? 256 : 128;
   const int mb = ceil_div(M, 128), nb = ceil_div(N, bn);
   if ((long long)G * mb * nb > INT_MAX / 2) return fail(DG_ERR_UNSUPPORTED, "too many tiles");
   const int tiles = G * mb * nb;
@@ -652,8 +655,8 @@ dg_status run_k_grouped(bool out_f32, const uint8_t* A, const float* sA, const u
   p.num_tiles = tiles;
   p.raster_m = (int16_t)(mb < 16 ? mb : 16);
   p.tail_splits = 1;   // every group's K range comes from its offsets
-  p.sA = sA;
-  p.sB = sB;
+  p.sA = static_cast<const float*>(sA);   // (packed UE8M0 words when block_scaled)
+  p.sB = static_cast<const float*>(sB);
   p.D = D;
   p.status = st->status;
   p.flags = dg::kFlagAMN | dg::kFlagBMN | wait_limit_flags();
@@ -677,9 +680,9 @@ dg_status run_k_grouped(bool out_f32, const uint8_t* A, const float* sA, const u
   a.grid = tiles < sms ? tiles : sms;
   a.stream = stream;
   if (print_configs())
-    std::fprintf(stderr, "[dg] k-grouped%s G=%d M=%d N=%d K_total=%d: BM=128 BN=%d grid=%d tiles=%d\n",
-                 out_f32 ? "/f32" : "", G, M, N, K_total, bn, a.grid, tiles);
-  const cudaError_t e = dg::launch_kgrouped(a);
+    std::fprintf(stderr, "[dg] k-grouped%s%s G=%d M=%d N=%d K_total=%d: BM=128 BN=%d grid=%d tiles=%d\n",
+                 block_scaled ? "/ue8m0" : "", out_f32 ? "/f32" : "", G, M, N, K_total, bn, a.grid, tiles);
+  const cudaError_t e = block_scaled ? dg::launch_bs_kgrouped(a) : dg::launch_kgrouped(a);
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
   return DG_OK;
 }
@@ -772,6 +775,18 @@ dg_status dg_fp8_k_grouped_gemm_tn_contiguous_f32(const uint8_t* A, const float*
                                                   const float* sB, const int32_t* k_offsets, float* D, int G, int M,
                                                   int N, int K_total, dg_stream_t stream) {
   return run_k_grouped(true, A, sA, B, sB, k_offsets, D, G, M, N, K_total, static_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                                    const int32_t* sB, const int32_t* k_offsets, uint16_t* D, int G,
+                                                    int M, int N, int K_total, dg_stream_t stream) {
+  return run_k_grouped(false, A, sA, B, sB, k_offsets, D, G, M, N, K_total, static_cast<cudaStream_t>(stream), true);
+}
+
+dg_status dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32(const uint8_t* A, const int32_t* sA, const uint8_t* B,
+                                                        const int32_t* sB, const int32_t* k_offsets, float* D, int G,
+                                                        int M, int N, int K_total, dg_stream_t stream) {
+  return run_k_grouped(true, A, sA, B, sB, k_offsets, D, G, M, N, K_total, static_cast<cudaStream_t>(stream), true);
 }
 
 dg_status dg_fp8_gemm_nn(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int M,

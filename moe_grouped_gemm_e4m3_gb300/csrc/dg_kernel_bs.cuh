@@ -182,7 +182,9 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
         const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
-        const int b_row = tile.g * p.N + tile.n_blk * BN;
+        // (K-grouped: B [K_total, N] is shared by the groups, and A's M coordinate is the m-block's)
+        const int b_row = (MODE == kKGrouped ? 0 : tile.g * p.N) + tile.n_blk * BN;
+        const int a_m = MODE == kKGrouped ? tile.m_blk * 128 : tile.a_row;
         int ok = 1;
         if (lane == 0) {
           for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++it) {
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
             uint8_t* sa = smem + s * Plan::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], Plan::kStageBytes);
             if (p.flags & kFlagAMN)   // A stored [K, M]: the box is 128 K-rows x 128 M-bytes
-              tma_load_2d(&tmA, sa, &full_bar[s], tile.a_row, kb * 128, policy);
+              tma_load_2d(&tmA, sa, &full_bar[s], a_m, kb * 128, policy);
             else
               tma_load_2d(&tmA, sa, &full_bar[s], kb * 128, tile.a_row, policy);
             if constexpr (SWIGLU) {
@@ -317,7 +319,10 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       for (int t = blockIdx.x; alive && t < total_tiles; t += gridDim.x) {
         const Tile tile = decode_tile<BN, MODE>(p, sc, t, lane);
         if (tile.skip) continue;
-        if (poster && !post(tile, 0)) { alive = false; break; }
+        // (an empty K range, possible in the K-grouped form, is posted as such: the epilogue stores
+        // zeros, and no scale slot is written for it)
+        if (poster && !post(tile, tile.kb1 <= tile.kb0 ? 2 : 0)) { alive = false; break; }
+        if (tile.kb1 <= tile.kb0) continue;
         const int row_in_tile = q * 32 + lane;
         const bool row_exists = row_in_tile < tile.rows;
         const int m_local = tile.m_blk * 128 + row_in_tile;
@@ -325,7 +330,8 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         // the tile's two 128-row scale blocks of B: 2n and 2n + 1, or (SwiGLU) gate block n and up
         // block I/128 + n
         const int nb0 = SWIGLU ? tile.n_blk : tile.n_blk * 2;
-        const uint32_t* sfb_ptr = reinterpret_cast<const uint32_t*>(p.sB) + ((size_t)tile.g * p.nnb + nb0) * nkq;
+        const uint32_t* sfb_ptr =
+            reinterpret_cast<const uint32_t*>(p.sB) + ((size_t)(MODE == kKGrouped ? 0 : tile.g) * p.nnb + nb0) * nkq;
         const uint32_t* sfb1_ptr = SWIGLU ? sfb_ptr + (size_t)(p.swiglu_i / 128) * nkq : sfb_ptr + nkq;
         const bool has_nb1 = SWIGLU || nb0 + 1 < p.nnb;
         const int q_end = (tile.kb1 - 1) >> 2;
@@ -383,7 +389,7 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
     static_assert(128 * kRowBytes <= STAGES * Plan::kStageBytes, "partial tile exceeds the stage buffers");
     while (alive) {
       // the next tile's description, copied into this warp's stash before its slot is released
-      bool active;
+      bool active, empty_k = false;
       {
         const uint32_t ds = desc_it % Plan::kDescSlots;
         if (!mbar_wait(&desc_full_bar[ds], (desc_it / Plan::kDescSlots) & 1, abort_flag, p.status, p.flags)) {
@@ -392,12 +398,13 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
         }
         ++desc_it;
         const volatile int* d = desc_ring + ds * 8;
-        const int end = d[7];
+        const int end = d[7];   // 1: no more tiles; 2: a tile with an empty K range (zeros)
         const int n_blk0 = d[2], rows0 = d[6];
         if (lane < 7) stash[lane] = d[lane];
         __syncwarp();
         if (lane == 0) mbar_arrive(&desc_empty_bar[ds]);
-        if (end) break;
+        if (end == 1) break;
+        empty_k = end == 2;
         active = (SWIGLU || n_blk0 * BN + cgrp * EPI_COLS < p.N) && __any_sync(0xffffffffu, row_in_tile < rows0);
       }
       // this warp's 32x128 block of the accumulator (live only within one tile)
@@ -426,6 +433,11 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty_bar);
+      if (empty_k) {
+        // an empty K range: nothing was accumulated (the tensor memory holds the previous tile)
+#pragma unroll
+        for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+      }
       Tile tile;
       tile.g = stash[0]; tile.m_blk = stash[1]; tile.n_blk = stash[2];
       tile.split = stash[3] & 0xFFFF; tile.splits = stash[3] >> 16;   // (split, splits) packed in one int

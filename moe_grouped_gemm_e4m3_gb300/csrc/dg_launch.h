@@ -41,6 +41,8 @@ cudaError_t launch_masked_swiglu(const LaunchArgs& a);
 cudaError_t launch_bs(const LaunchArgs& a, Mode mode);
 // The block-scaled masked form fused with SwiGLU.
 cudaError_t launch_bs_swiglu(const LaunchArgs& a);
+// The block-scaled K-grouped form (MN-major A and B).
+cudaError_t launch_bs_kgrouped(const LaunchArgs& a);
 // How many clusters of `cluster` CTAs of the dense / contiguous instantiation for (block_n,
 // out_f32) can be resident at once (0 if the query fails).
 int cluster_capacity_dense(int block_n, bool out_f32, int cluster);

@@ -176,3 +176,8 @@ def test_k_grouped_shapes():
     _refused(fn, args, 3, f32(cdiv(NG, 128), KT // 128 - 1))
     _refused(fn, args, 5, bf16(G + 1, MG, NG))             # D's group count follows k_offsets
     _refused(fn, args, 4, i32(G + 1, 1))                   # k_offsets not 1-D
+    nkq = cdiv(KT // 128, 4)
+    pargs = [u8(KT, MG), i32(nkq, a4(MG)), u8(KT, NG), i32(cdiv(NG, 128), nkq), i32(G + 1), bf16(G, MG, NG)]
+    _accepted(dg.dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0, pargs)
+    _refused(dg.dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0, pargs, 1, i32(KT // 128, a4(MG)))
+    _refused(dg.dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0, pargs, 3, i32(cdiv(NG, 128), KT // 128))

@@ -147,3 +147,14 @@ def test_timeout_block_scaled(dg, M, N, K):
     A, sA, B, sB = dev(a.A), dev(pa), dev(b.B[0]), dev(pb[0])
     D = bf16_sentinel((M, N))
     _timeout_then_recover(dg, lambda: dg.dg_fp8_gemm_nt_ue8m0(A, sA, B, sB, D), D)
+
+
+def test_timeout_k_grouped_ue8m0(dg):
+    M, N, off = 512, 1024, np.array([0, 1024, 1024, 3072], np.int32)
+    K = int(off[-1])
+    a = dg_inputs.make_a(M, K, seed=10, ue8m0=True)
+    b = dg_inputs.make_b(1, N, K, seed=10, ue8m0=True)
+    A, B = dev(np.ascontiguousarray(a.A.T)), dev(np.ascontiguousarray(b.B[0].T))
+    sA, sB, O = dev(dg_inputs.pack_ue8m0_a(a.sA)), dev(dg_inputs.pack_ue8m0_b(b.sB)[0]), dev(off)
+    D = bf16_sentinel((len(off) - 1, M, N))
+    _timeout_then_recover(dg, lambda: dg.dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0(A, sA, B, sB, O, D), D)
