@@ -833,6 +833,14 @@ def run_all_configs(args):
             nbytes = valid * K + active * N2 * K + 4 * valid * nks + 4 * G * (N2 // 128) * nks + 2 * valid * I
             report("7 masked + SwiGLU (fused)", f"G=16 M_max=256 sum(masked_m)={valid} 2I={N2} K={K}",
                    2.0 * valid * N2 * K, nbytes, ms, dict(scales))
+            if not UE8M0:   # H cast to FP8 in the epilogue (1x128 groups): the down projection's A and sA
+                Hq = torch.empty(G, M_max, I, dtype=torch.uint8, device="cuda")
+                sH = torch.empty(G, I // 128, -(-M_max // 4) * 4, dtype=torch.float32, device="cuda")
+                ms = timeit(lambda: dg.dg_fp8_grouped_masked_swiglu_fp8(A, sA, B, sB, MM, Hq, sH))
+                nbytes += -2 * valid * I + valid * I + 4 * valid * (I // 128)
+                report("7 masked + SwiGLU + FP8 H (fused)", f"G=16 M_max=256 sum(masked_m)={valid} 2I={N2} K={K}",
+                       2.0 * valid * N2 * K, nbytes, ms, dict(scales))
+                del Hq, sH
             del A, B, H
     # the NN / TN / TT layouts (both scale forms): A stored [K,M] and/or B stored [K,N]
     if want(8):

@@ -263,6 +263,20 @@ dg_status dg_fp8_grouped_masked_swiglu(const uint8_t* A, const float* sA, const 
 dg_status dg_fp8_grouped_masked_swiglu_f32(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                                            const int32_t* masked_m, float* H, int G, int M_max, int N, int K,
                                            dg_stream_t stream);
+/* The fused SwiGLU with H cast to FP8 for the down projection. The Mega MoE kernel runs linear 1,
+   the SwiGLU and linear 2 back to back, and linear 2 takes FP8 activations ("DeepGEMM: İnce
+   ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri", tr.news.hada.io/topic?id=19459,
+   § "Mega MoE"); the cast between them is this call. Arguments as dg_fp8_grouped_masked_swiglu,
+   except the output: for each valid row m < masked_m[g] and each 1x128 group j of H's I columns,
+   sH[g][j][m] = amax/448 (FP32, IEEE division; 1 where amax = 0) over that row's 128 values of
+   H = silu(gate)·up (the FP32 values dg_fp8_grouped_masked_swiglu_f32 produces), and
+   Hq[g][m][128j + c] = e4m3_rne(clamp(H / sH, ±448)) (IEEE FP32 division, round to nearest
+   even). Hq is [G][M_max][I] bytes, sH is [G][I/128][align4(M_max)] FP32: exactly the A and sA
+   layouts dg_fp8_grouped_masked takes, so the down projection consumes them as they are. Rows
+   past masked_m are untouched in both. Hq must be 16-byte aligned, sH 4-byte aligned. */
+dg_status dg_fp8_grouped_masked_swiglu_fp8(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                           const int32_t* masked_m, uint8_t* Hq, float* sH, int G, int M_max, int N,
+                                           int K, dg_stream_t stream);
 /* The fused SwiGLU with power-of-two scales packed as UE8M0, on the block-scaled kernel: the layouts
    of A, B, masked_m and H as for dg_fp8_grouped_masked_swiglu, the packed scale layouts of
    dg_fp8_grouped_masked_ue8m0 (sA [G][ceil(ceil(K/128)/4)][align4(M_max)], sB [G][N/128][ceil(ceil(K/128)/4)],

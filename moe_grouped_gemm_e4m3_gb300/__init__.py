@@ -40,7 +40,8 @@ __all__ = [
     "dg_set_tail_splits", "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
-    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_ue8m0",
+    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_fp8",
+    "dg_fp8_grouped_masked_swiglu_ue8m0",
     "dg_fp8_grouped_masked_swiglu_ue8m0_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
     "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32",
@@ -63,7 +64,8 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
-    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_ue8m0",
+    "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_fp8",
+    "dg_fp8_grouped_masked_swiglu_ue8m0",
     "dg_fp8_grouped_masked_swiglu_ue8m0_f32", "dg_fp8_gemm_nn", "dg_fp8_gemm_nn_f32",
     "dg_fp8_gemm_tn", "dg_fp8_gemm_tn_f32", "dg_fp8_gemm_tt", "dg_fp8_gemm_tt_f32",
     "dg_fp8_gemm_nn_ue8m0", "dg_fp8_gemm_nn_ue8m0_f32", "dg_fp8_gemm_tn_ue8m0", "dg_fp8_gemm_tn_ue8m0_f32", "dg_fp8_gemm_tt_ue8m0", "dg_fp8_gemm_tt_ue8m0_f32",
@@ -108,6 +110,8 @@ def load(build_if_missing: bool = True):
                  "dg_fp8_grouped_masked_swiglu_ue8m0_f32"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, P, P, P, P, i32, i32, i32, i32, P]
+    lib.dg_fp8_grouped_masked_swiglu_fp8.restype = i32
+    lib.dg_fp8_grouped_masked_swiglu_fp8.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, P]
     lib.dg_get_tma_aligned_size.restype, lib.dg_get_tma_aligned_size.argtypes = i32, [i32, i32]
     lib.dg_get_mk_alignment_for_contiguous_layout.restype = i32
     lib.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
@@ -470,6 +474,33 @@ def dg_fp8_grouped_masked_swiglu(A, sA, B, sB, masked_m, H, stream=None):
 
 def dg_fp8_grouped_masked_swiglu_f32(A, sA, B, sB, masked_m, H, stream=None):
     return _masked("dg_fp8_grouped_masked_swiglu_f32", True, A, sA, B, sB, masked_m, H, stream)
+
+
+def dg_fp8_grouped_masked_swiglu_fp8(A, sA, B, sB, masked_m, Hq, sH, stream=None):
+    """The fused SwiGLU with H cast to FP8 for the down projection: Hq [G, M_max, I] E4M3 codes
+    (uint8 or float8_e4m3fn) and sH [G, I/128, align4(M_max)] float32, one scale amax/448 per 1x128
+    group of each valid row; the A and sA layouts of dg_fp8_grouped_masked. Rows past masked_m are
+    untouched in both."""
+    import torch
+    a, b = _shape(A, "A"), _shape(B, "B")
+    if len(a) != 3 or len(b) != 3:
+        raise ValueError(f"masked layout: A must be [G, M_max, K] and B [G, 2I, K], got {list(a)} and {list(b)}")
+    G, M_max, K = a
+    N = b[1]
+    if b[0] != G or b[2] != K:
+        raise ValueError(f"B has shape {list(b)}, expected [{G}, 2I, {K}]")
+    nkb = _cdiv(K, 128)
+    _expect(sA, "sA", (G, nkb, _align4(M_max)))
+    _expect(sB, "sB", (G, _cdiv(N, 128), nkb))
+    _expect(masked_m, "masked_m", (G,))
+    _expect(Hq, "Hq", (G, M_max, N // 2))
+    _expect(sH, "sH", (G, (N // 2) // 128, _align4(M_max)))
+    lib = load()
+    _check(lib.dg_fp8_grouped_masked_swiglu_fp8(
+        _ptr(A, "A", _fp8_types()), _ptr(sA, "sA", _f32()), _ptr(B, "B", _fp8_types()), _ptr(sB, "sB", _f32()),
+        _ptr(masked_m, "masked_m", (torch.int32,)), _ptr(Hq, "Hq", _fp8_types()), _ptr(sH, "sH", _f32()),
+        G, M_max, N, K, _stream(stream)))
+    return Hq, sH
 
 
 def dg_fp8_grouped_masked_swiglu_ue8m0(A, sA, B, sB, masked_m, H, stream=None):

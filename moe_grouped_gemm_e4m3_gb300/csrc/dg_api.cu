@@ -408,8 +408,14 @@ dg_status noalloc_scratch(void** out);
 dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, const uint8_t* B, const void* sB,
                    const int32_t* idx, void* D, int rows, int N, int K, int G, cudaStream_t stream,
                    bool block_scaled = false, const float* C = nullptr, bool accumulate = false,
-                   bool swiglu = false, bool a_mn = false, bool b_mn = false, bool noalloc = false) {
+                   bool swiglu = false, bool a_mn = false, bool b_mn = false, bool noalloc = false,
+                   float* h_scales = nullptr) {
   t_last_error.clear();
+  // h_scales: the fused SwiGLU writes H as FP8 codes (D, bytes) and these 1x128-group scales
+  const bool quant_h = h_scales != nullptr;
+  if (quant_h && (!swiglu || out_f32 || block_scaled))
+    return fail(DG_ERR_INVALID_ARG, "FP8 H: the fused SwiGLU with FP32 scales");
+  if (quant_h && !aligned(h_scales, 4)) return fail(DG_ERR_ALIGNMENT, "sH must be 4-byte aligned");
   if (rows < 0 || N < 0 || K < 0 || G < 0) return fail(DG_ERR_INVALID_ARG, "negative size");
   if (mode != dg::kDense && G < 1 && rows > 0) {
     if (G == 0) return DG_OK;
@@ -417,11 +423,11 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   if (accumulate && (!C || !out_f32 || mode != dg::kDense))
     return fail(DG_ERR_INVALID_ARG, "the accumulating form needs a C pointer and FP32 D (dense only)");
   if (swiglu && (mode != dg::kMasked || accumulate))
-    return fail(DG_ERR_INVALID_ARG, "the fused SwiGLU form is masked, with FP32 scales");
+    return fail(DG_ERR_INVALID_ARG, "the fused SwiGLU form is masked and not accumulating");
   if (swiglu && N % 256 != 0)
     return fail(DG_ERR_ALIGNMENT, "fused SwiGLU: B must hold 2I rows per group with I a multiple of 128");
   if ((a_mn || b_mn) && mode != dg::kDense)
-    return fail(DG_ERR_INVALID_ARG, "the NN/TN/TT layouts are dense, with FP32 scales");
+    return fail(DG_ERR_INVALID_ARG, "the NN/TN/TT layouts are dense");
   if (rows == 0 || N == 0 || G == 0) return DG_OK;
   if (K == 0) return fail(DG_ERR_INVALID_ARG, "K must be positive");
   if (!A || !sA || !B || !sB || !D) return fail(DG_ERR_INVALID_ARG, "null tensor pointer");
@@ -497,6 +503,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.masked_m = mode == dg::kMasked ? idx : nullptr;
   p.D = D;
   p.status = st->status;
+  if (quant_h) p.workspace = h_scales;   // (the fused SwiGLU has no split-K workspace)
   if (accumulate && static_cast<const void*>(C) != D) {
     cudaError_t ce = cudaMemcpyAsync(D, C, (size_t)rows * N * sizeof(float), cudaMemcpyDeviceToDevice, stream);
     if (ce != cudaSuccess) return fail_cuda(ce, "cudaMemcpyAsync(C -> D)");
@@ -565,7 +572,10 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != DG_OK) {
     return s;
   }
-  if (out_f32) {
+  if (quant_h) {   // (FP8 H is written with plain stores; the map only has to be valid)
+    s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, (uint64_t)d_cols, (uint64_t)rows_total, (uint64_t)d_cols,
+                  32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "H");
+  } else if (out_f32) {
     s = encode_2d(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, (uint64_t)d_cols, (uint64_t)rows_total,
                   (uint64_t)d_cols * 4, 16, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "D", CU_TENSOR_MAP_SWIZZLE_64B);
   } else {
@@ -587,7 +597,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   }
   cudaError_t e;
   if (swiglu) {
-    e = block_scaled ? dg::launch_bs_swiglu(a) : dg::launch_masked_swiglu(a);
+    e = block_scaled ? dg::launch_bs_swiglu(a) : dg::launch_masked_swiglu(a, quant_h);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return DG_OK;
   }
@@ -873,6 +883,14 @@ dg_status dg_fp8_grouped_masked_swiglu_f32(const uint8_t* A, const float* sA, co
                                            dg_stream_t stream) {
   return run_gemm(dg::kMasked, true, A, sA, B, sB, masked_m, H, M_max, N, K, G, static_cast<cudaStream_t>(stream),
                   false, nullptr, false, true);
+}
+
+dg_status dg_fp8_grouped_masked_swiglu_fp8(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                           const int32_t* masked_m, uint8_t* Hq, float* sH, int G, int M_max, int N,
+                                           int K, dg_stream_t stream) {
+  if (!sH) return fail(DG_ERR_INVALID_ARG, "null sH");
+  return run_gemm(dg::kMasked, false, A, sA, B, sB, masked_m, Hq, M_max, N, K, G, static_cast<cudaStream_t>(stream),
+                  false, nullptr, false, true, false, false, false, sH);
 }
 
 dg_status dg_fp8_grouped_masked_swiglu_ue8m0(const uint8_t* A, const int32_t* sA, const uint8_t* B, const int32_t* sB,

@@ -93,6 +93,14 @@ constexpr int kFlagClusterSplit = 0x8;
 // which TMA multicasts into both CTAs' shared memory, so each SM pulls a third less from L2 per
 // K-block. Every MMA commit then releases the stage in both CTAs (empty barriers count 2).
 constexpr int kFlagPairB = 0x10;
+// The SWIGLU template argument: 0 no SwiGLU; kSwiglu H = silu(gate)·up stored as BF16/FP32;
+// kSwigluFp8 H quantised to FP8 for the down projection: each row's 128 columns of a tile (one 1x128
+// group) get the scale s = amax/448 (1 where amax = 0) and the codes e4m3_rne(clamp(h / s, ±448)).
+// D then points to the codes [G·M_max, I] (bytes) and workspace to the scales [G][I/128][ldsa]
+// (the MN-major LHS scale layout of the masked GEMM). A separate instantiation, because the
+// correctly rounded divisions raise the epilogue's register pressure.
+constexpr int kSwiglu = 1;
+constexpr int kSwigluFp8 = 2;
 // Bits 8..31 of the flags word hold the time limit of the pipeline waits in microseconds
 // (kWaitLimitShift, mbar_wait).
 
@@ -414,7 +422,7 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // and the 128 up rows I + 128·n ..; the epilogue pairs the two halves and stores
 // H = silu(gate)·up, 128 columns of the [G·M_max, I] output per tile.
 
-template <int BN, int EPI_COLS, int STAGES, int NBUF, Mode MODE, bool OUT_F32, bool SWIGLU>
+template <int BN, int EPI_COLS, int STAGES, int NBUF, Mode MODE, bool OUT_F32, int SWIGLU>
 __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
@@ -905,6 +913,12 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&xempty_bar[quad]);   // the up warp may refill the buffer
+          if constexpr (SWIGLU == kSwigluFp8) {
+            // keep H in place of the gate values until the row's 128 columns are all formed
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[r * 32 + j] = h[j];
+            continue;
+          }
           if (all_rows) {
 #pragma unroll
             for (int box = 0; box < 32 / kColsPerBox; ++box) {
@@ -959,6 +973,27 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           }
         }
         if (!ok) { alive = false; break; }
+        if (SWIGLU == kSwigluFp8 && cgrp == 0 && row_exists) {
+          // the row's 128 columns of H are one 1x128 group: its scale, then its FP8 codes
+          float amax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 128; ++j) amax = fmaxf(amax, fabsf(acc[j]));
+          const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+          uint8_t* qrow = reinterpret_cast<uint8_t*>(p.D) + (size_t)(tile.a_row + row_in_tile) * p.swiglu_i + h_col0;
+#pragma unroll
+          for (int j = 0; j < 128; j += 16) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int c = j + q * 4;
+              const uint32_t lo = e4m3x2_satfinite(__fdiv_rn(acc[c], sc), __fdiv_rn(acc[c + 1], sc));
+              const uint32_t hi = e4m3x2_satfinite(__fdiv_rn(acc[c + 2], sc), __fdiv_rn(acc[c + 3], sc));
+              w[q] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4*>(qrow + j) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          p.workspace[((size_t)tile.g * (p.swiglu_i / 128) + tile.n_blk) * p.ldsa + m_local] = sc;
+        }
         continue;
       }
 

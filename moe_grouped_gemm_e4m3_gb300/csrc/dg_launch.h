@@ -35,8 +35,9 @@ cudaError_t launch_contiguous(const LaunchArgs& a);
 cudaError_t launch_masked(const LaunchArgs& a);
 // The K-grouped form (groups along K; FP32-scale kernel, MN-major A and B).
 cudaError_t launch_kgrouped(const LaunchArgs& a);
-// The masked form fused with SwiGLU (block_n 256, FP32-scale kernel).
-cudaError_t launch_masked_swiglu(const LaunchArgs& a);
+// The masked form fused with SwiGLU (block_n 256, FP32-scale kernel); fp8_h: H as FP8 codes and
+// 1x128-group scales.
+cudaError_t launch_masked_swiglu(const LaunchArgs& a, bool fp8_h = false);
 // The block-scaled kernel for packed UE8M0 scales (block_n is always 256).
 cudaError_t launch_bs(const LaunchArgs& a, Mode mode);
 // The block-scaled masked form fused with SwiGLU.
@@ -95,7 +96,7 @@ int clusters_resident(Kernel kernel, int threads, size_t smem_bytes, int cluster
 }
 
 // Launches one instantiation; sets its dynamic shared-memory limit on first use per device.
-template <int BN, Mode MODE, bool OUT_F32, bool SWIGLU = false>
+template <int BN, Mode MODE, bool OUT_F32, int SWIGLU = 0>
 cudaError_t launch_instance(const LaunchArgs& a) {
   constexpr int STAGES = stages_for(BN);
   constexpr int EPI_COLS = epi_cols_for(BN);

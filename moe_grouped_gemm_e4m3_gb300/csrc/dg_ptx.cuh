@@ -5,6 +5,8 @@
 
 #include <cstdint>
 
+#include <cuda_fp8.h>
+
 namespace dg {
 
 // ---------------------------------------------------------------------------------------------
@@ -141,6 +143,12 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+
+// Two FP32 values as E4M3 codes (round to nearest even, saturating to ±448), `first` in the low
+// byte, through CUDA's conversion intrinsic.
+__device__ __forceinline__ uint32_t e4m3x2_satfinite(float first, float second) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(first, second), __NV_SATFINITE, __NV_E4M3);
 }
 
 // Largest cluster the split-K exchange uses (the portable cluster size).

@@ -180,6 +180,44 @@ def silu(x) -> np.ndarray:
     return np.array([lib.dgo_silu(float(v)) for v in x.ravel()], np.float64).reshape(x.shape)
 
 
+def e4m3_encode_rne(y) -> np.ndarray:
+    """E4M3 code of each FP32 value y with |y| <= 448: the representable value nearest to y (the
+    finite values of the OCP table, from ``e4m3_decode``), a tie going to the even code (even
+    mantissa), the sign of y kept (a negative value that rounds to zero gives -0, code 0x80).
+    Values beyond ±448 must have been clamped by the caller."""
+    y = np.asarray(y, np.float32)
+    if np.any(np.abs(y) > 448.0) or np.any(np.isnan(y)):
+        raise ValueError("e4m3_encode_rne takes finite values with |y| <= 448")
+    codes = np.arange(0, 127, dtype=np.uint8)                 # 0x00..0x7E: +0 .. 448
+    vals = e4m3_decode(codes)                                  # increasing
+    a = np.abs(y.astype(np.float64)).ravel()
+    hi = np.searchsorted(vals, a, side="left")                 # vals[hi-1] < a <= vals[hi]
+    hi = np.clip(hi, 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick = np.where(d_hi < d_lo, hi, np.where(d_lo < d_hi, lo, np.where(codes[hi] % 2 == 0, hi, lo)))
+    out = codes[pick].astype(np.uint8)
+    out = np.where(np.signbit(y.ravel()), out | np.uint8(0x80), out).astype(np.uint8)
+    return out.reshape(y.shape)
+
+
+def quantize_rows_e4m3(H, group: int = 128):
+    """FP8 cast of H [..., R, C] per 1 x ``group`` group of each row: s = amax/448 in FP32 (1 where
+    amax = 0), codes = e4m3_rne(clamp(H / s, ±448)) with the FP32 division. Returns (codes [..., R, C]
+    uint8, scales [..., C/group, R] float32: the MN-major LHS scale layout, unpadded)."""
+    H = np.asarray(H, np.float32)
+    *lead, R, C = H.shape
+    if C % group:
+        raise ValueError("the row length must be a multiple of the group")
+    Hg = H.reshape(*lead, R, C // group, group)
+    amax = np.max(np.abs(Hg), axis=-1)                                     # [..., R, C/group] FP32
+    s = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0)).astype(np.float32)
+    y = (Hg / s[..., None]).astype(np.float32)                            # FP32 (IEEE) division
+    y = np.clip(y, np.float32(-448.0), np.float32(448.0))
+    codes = e4m3_encode_rne(y).reshape(*lead, R, C)
+    return codes, np.swapaxes(s, -1, -2).copy()
+
+
 def grouped_masked_swiglu(A, sA, B, sB, masked_m, ref64_init=None, H_init=None, threads=None):
     """Masked grouped GEMM fused with SwiGLU: B [G, 2I, K] (gate rows then up rows),
     H[g,m,j] = silu(D[g,m,j])·D[g,m,I+j] for m < masked_m[g]. Returns (ref64, H bf16 bits, n_clamped)."""

@@ -132,6 +132,11 @@ def test_swiglu_shapes():
     _accepted(dg.dg_fp8_grouped_masked_swiglu_ue8m0_f32, pargs[:5] + [f32(G, MM, N2 // 2)])
     _refused(dg.dg_fp8_grouped_masked_swiglu_ue8m0, pargs, 1, i32(G, NKB, a4(MM)))
     _refused(dg.dg_fp8_grouped_masked_swiglu_ue8m0, pargs, 5, bf16(G, MM, N2))
+    qargs = args[:5] + [u8(G, MM, N2 // 2), f32(G, N2 // 256, a4(MM))]
+    _accepted(dg.dg_fp8_grouped_masked_swiglu_fp8, qargs)
+    _refused(dg.dg_fp8_grouped_masked_swiglu_fp8, qargs, 5, u8(G, MM, N2))       # Hq is I wide
+    _refused(dg.dg_fp8_grouped_masked_swiglu_fp8, qargs, 6, f32(G, N2 // 128, a4(MM)))   # sH has I/128 groups
+    _refused(dg.dg_fp8_grouped_masked_swiglu_fp8, qargs, 6, f32(G, N2 // 256, MM + 1))
 
 
 @pytest.mark.parametrize("layout", ["nn", "tn", "tt"])

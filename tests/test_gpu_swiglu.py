@@ -100,3 +100,81 @@ def test_swiglu_rejects_bad_width(dg):
     with pytest.raises(dg.DGError) as e:
         dg.dg_fp8_grouped_masked_swiglu(dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(np.array([5, 6], np.int32)), H)
     assert e.value.status == dg.DG_ERR_ALIGNMENT
+
+
+# ----------------------------------------------------------------------------------------------
+# The fused SwiGLU with H cast to FP8 (dg_fp8_grouped_masked_swiglu_fp8). The cast is a decision
+# per element, so it is checked in the kernel's own precision: the codes and scales must equal,
+# bit for bit, the oracle's plain 1x128 quantiser applied to the FP32 H of the same kernel
+# (dg_fp8_grouped_masked_swiglu_f32). The dequantised H is checked against the FP64 oracle within
+# half an E4M3 step of each group's top binade, and the down projection consumes Hq/sH as its A/sA.
+
+def _align4(x):
+    return -(-x // 4) * 4
+
+
+def _fp8_h(dg, a, b, masked_m):
+    G, M_max, _ = a.A.shape
+    I = b.B.shape[1] // 2
+    Hq = torch.full((G, M_max, I), 0x7F, dtype=torch.uint8, device="cuda")          # NaN codes
+    sH = torch.full((G, I // 128, _align4(M_max)), float("nan"), dtype=torch.float32, device="cuda")
+    dg.dg_fp8_grouped_masked_swiglu_fp8(dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(masked_m), Hq, sH)
+    torch.cuda.synchronize()
+    return Hq.cpu().numpy(), sH.cpu().numpy()
+
+
+def _check_fp8_h(dg, a, b, masked_m, label, ref64=None):
+    G, M_max, _ = a.A.shape
+    I = b.B.shape[1] // 2
+    _, H32 = _run(dg, a, b, masked_m)
+    Hq, sH = _fp8_h(dg, a, b, masked_m)
+    valid = _valid(masked_m, M_max)
+    h32 = H32.cpu().numpy()
+    h32 = np.where(valid[..., None], h32, 0.0).astype(np.float32)
+    codes, scales = oracle.quantize_rows_e4m3(h32)          # scales [G, I/128, M_max]
+    assert np.all(Hq[~valid] == 0x7F), f"{label}: rows past masked_m were written"
+    assert np.array_equal(Hq[valid], codes[valid]), f"{label}: codes differ from the 1x128 cast of H"
+    sv = np.swapaxes(sH[:, :, :M_max], 1, 2)                # [G, M_max, I/128]
+    assert np.all(np.isnan(sv[~valid])) and np.all(np.isnan(sH[:, :, M_max:]))
+    assert np.array_equal(sv[valid].view(np.int32), np.swapaxes(scales, 1, 2)[valid].view(np.int32)), \
+        f"{label}: scales differ"
+    if ref64 is not None:
+        deq = oracle.e4m3_decode(Hq).reshape(G, M_max, I // 128, 128) * sv[..., None]
+        h64 = ref64.reshape(G, M_max, I // 128, 128)
+        amax = np.max(np.abs(h32.reshape(G, M_max, I // 128, 128)), axis=-1, keepdims=True)
+        bound = (16.0 / 448.0) * amax * 1.0001 + 2e-3 * np.max(np.abs(ref64))
+        assert np.all(np.abs(deq - h64)[valid] <= bound[valid]), f"{label}: dequantised H off the oracle"
+    return Hq, sH
+
+
+@pytest.mark.parametrize("I,K", [(128, 384), (256, 1024), (384, 256)])
+def test_swiglu_fp8_h_full(dg, I, K):
+    masked_m = np.array([0, 1, 127, 128, 129, 256], np.int32)
+    G, M_max = len(masked_m), 256
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=43)
+    b = dg_inputs.make_b(G, 2 * I, K, seed=43)
+    ref, _, bad = oracle.grouped_masked_swiglu(a.A, a.sA, b.B, b.sB, masked_m)
+    assert bad == 0
+    _check_fp8_h(dg, a, b, masked_m, f"fp8 H I={I} K={K}", ref64=ref)
+
+
+def test_swiglu_fp8_h_decode_and_down_projection(dg):
+    G, M_max, I, K, N2 = 16, 256, 2048, 7168, 1024
+    masked_m = dg_inputs.make_masked_m(G, M_max, seed=0)
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=0)
+    b = dg_inputs.make_b(G, 2 * I, K, seed=0)
+    Hq, sH = _check_fp8_h(dg, a, b, masked_m, "fp8 H decode")
+    # the down projection reads Hq and sH as its A and sA, exactly as they are
+    w2 = dg_inputs.make_b(G, N2, I, seed=2)
+    D2 = bf16_sentinel((G, M_max, N2))
+    D2_32 = f32_sentinel((G, M_max, N2))
+    args = (dev(Hq), dev(np.ascontiguousarray(sH)), dev(w2.B), dev(w2.sB), dev(masked_m))
+    dg.dg_fp8_grouped_masked(*args, D2)
+    dg.dg_fp8_grouped_masked_f32(*args, D2_32)
+    torch.cuda.synchronize()
+    valid = _valid(masked_m, M_max)
+    ref2, _, bad = oracle.grouped_masked(Hq, sH, w2.B, w2.sB, masked_m)
+    assert bad == 0
+    db = bits16(D2).cpu()
+    assert torch.all(db[~torch.from_numpy(valid)] == -1)
+    assert_accurate(D2_32.cpu().numpy()[valid], db.numpy()[valid], ref2[valid], "down projection of FP8 H")

@@ -521,3 +521,59 @@ def test_k_grouped_equals_dense_on_slices():
     assert np.allclose(ref.sum(axis=0), full, rtol=1e-12, atol=1e-12 * np.abs(full).max())
     with pytest.raises(ValueError):
         oracle.k_grouped(a.A, a.sA, b.B[0], b.sB[0], np.array([0, 100, K], np.int32))
+
+
+# ----------------------------------------------------------------------------------------------
+# The FP8 cast of H (e4m3_encode_rne, quantize_rows_e4m3), the reference of the fused SwiGLU with
+# FP8 output: pinned against the OCP table round trip, torch's own float32 -> float8_e4m3fn
+# conversion (round to nearest even), hand-worked ties and closed forms of the 1x128 scale rule.
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)   # all but the NaNs
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    back = oracle.e4m3_encode_rne(vals)
+    # +0 and -0 keep their sign; every other code comes back as itself
+    assert np.array_equal(back, codes)
+
+
+def test_e4m3_encode_matches_torch_and_ties_go_to_even():
+    rng = np.random.default_rng(0)
+    y = np.concatenate([rng.uniform(-448, 448, 50000), rng.normal(0, 1e-2, 50000)]).astype(np.float32)
+    ours = oracle.e4m3_encode_rne(y)
+    ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    # every midpoint between adjacent representable magnitudes goes to the even code
+    vals = oracle.e4m3_decode(np.arange(127, dtype=np.uint8))
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mids.astype(np.float64), (vals[:-1] + vals[1:]) / 2)   # exact in FP32
+    want = np.where(np.arange(126) % 2 == 0, np.arange(126), np.arange(1, 127)).astype(np.uint8)
+    assert np.array_equal(oracle.e4m3_encode_rne(mids), want)
+    assert np.array_equal(oracle.e4m3_encode_rne(-mids), want | 0x80)
+    # worked by hand: 1.0625 lies between 1.0 (0x38) and 1.125 (0x39) -> 0x38; 1.1875 between
+    # 1.125 (0x39) and 1.25 (0x3A) -> 0x3A; 2^-10, half the smallest subnormal -> +0
+    assert list(oracle.e4m3_encode_rne(np.array([1.0625, 1.1875, 2.0 ** -10], np.float32))) == [0x38, 0x3A, 0x00]
+
+
+def test_quantize_rows_scale_rule_closed_forms():
+    rng = np.random.default_rng(1)
+    # a row whose group maximum is 448 has scale exactly 1: the codes are the values' own codes
+    vals = oracle.e4m3_decode(rng.integers(0, 126, 256).astype(np.uint8)).astype(np.float32)
+    vals[0], vals[128] = 448.0, -448.0
+    codes, s = oracle.quantize_rows_e4m3(vals[None, :])
+    assert s.shape == (2, 1) and np.all(s == 1.0)
+    assert np.array_equal(codes[0], oracle.e4m3_encode_rne(vals))
+    # an all-zero group has scale 1 and codes 0; the other group is unaffected by it
+    h = rng.normal(0, 3, (3, 256)).astype(np.float32)
+    h[1, :128] = 0.0
+    codes, s = oracle.quantize_rows_e4m3(h)
+    assert s[0, 1] == 1.0 and np.all(codes[1, :128] == 0)
+    assert s[1, 1] == np.float32(np.max(np.abs(h[1, 128:]))) / np.float32(448.0)
+    # scaling a group by a power of two scales its scale (the all-zero group keeps 1) and leaves its
+    # codes as they are
+    codes2, s2 = oracle.quantize_rows_e4m3(h * np.float32(2.0 ** -7))
+    want = np.where(np.swapaxes(np.max(np.abs(h.reshape(3, 2, 128)), axis=-1), 0, 1) > 0, s * np.float32(2.0 ** -7), 1.0)
+    assert np.array_equal(codes2, codes) and np.array_equal(s2, want.astype(np.float32))
+    # dequantised values are within half an E4M3 step of the top binade of each group
+    deq = oracle.e4m3_decode(codes).reshape(3, 2, 128) * np.swapaxes(s, 0, 1)[..., None]
+    err = np.abs(deq - h.reshape(3, 2, 128).astype(np.float64))
+    assert np.all(err <= (16.0 / 448.0) * np.max(np.abs(h.reshape(3, 2, 128)), axis=-1, keepdims=True) * 1.0001)
