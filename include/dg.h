@@ -268,10 +268,11 @@ dg_status dg_fp8_grouped_masked_swiglu_f32(const uint8_t* A, const float* sA, co
    ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri", tr.news.hada.io/topic?id=19459,
    § "Mega MoE"); the cast between them is this call. Arguments as dg_fp8_grouped_masked_swiglu,
    except the output: for each valid row m < masked_m[g] and each 1x128 group j of H's I columns,
-   sH[g][j][m] = amax/448 (FP32, IEEE division; 1 where amax = 0) over that row's 128 values of
-   H = silu(gate)·up (the FP32 values dg_fp8_grouped_masked_swiglu_f32 produces), and
-   Hq[g][m][128j + c] = e4m3_rne(clamp(H / sH, ±448)) (IEEE FP32 division, round to nearest
-   even). Hq is [G][M_max][I] bytes, sH is [G][I/128][align4(M_max)] FP32: exactly the A and sA
+   with amax the largest |H| over that row's 128 values of H = silu(gate)·up (the FP32 values
+   dg_fp8_grouped_masked_swiglu_f32 produces), Hq[g][m][128j + c] = e4m3_rne(clamp(H · (448/amax),
+   ±448)) (the factor 448/amax an IEEE FP32 division, the product rounded to nearest even in FP32,
+   then to the nearest E4M3 value, ties to even) and sH[g][j][m] = amax/448 (IEEE FP32 division),
+   the scale that dequantises the codes; an all-zero group has codes 0 and sH = 1. Hq is [G][M_max][I] bytes, sH is [G][I/128][align4(M_max)] FP32: exactly the A and sA
    layouts dg_fp8_grouped_masked takes, so the down projection consumes them as they are. Rows
    past masked_m are untouched in both. Hq must be 16-byte aligned, sH 4-byte aligned. */
 dg_status dg_fp8_grouped_masked_swiglu_fp8(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,

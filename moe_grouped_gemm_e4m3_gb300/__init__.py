@@ -478,8 +478,9 @@ def dg_fp8_grouped_masked_swiglu_f32(A, sA, B, sB, masked_m, H, stream=None):
 
 def dg_fp8_grouped_masked_swiglu_fp8(A, sA, B, sB, masked_m, Hq, sH, stream=None):
     """The fused SwiGLU with H cast to FP8 for the down projection: Hq [G, M_max, I] E4M3 codes
-    (uint8 or float8_e4m3fn) and sH [G, I/128, align4(M_max)] float32, one scale amax/448 per 1x128
-    group of each valid row; the A and sA layouts of dg_fp8_grouped_masked. Rows past masked_m are
+    (uint8 or float8_e4m3fn), e4m3_rne(H · (448/amax)), and sH [G, I/128, align4(M_max)] float32, the
+    dequantisation scale amax/448 of each 1x128 group of each valid row; the A and sA layouts of
+    dg_fp8_grouped_masked. Rows past masked_m are
     untouched in both."""
     import torch
     a, b = _shape(A, "A"), _shape(B, "B")

@@ -95,10 +95,11 @@ constexpr int kFlagClusterSplit = 0x8;
 constexpr int kFlagPairB = 0x10;
 // The SWIGLU template argument: 0 no SwiGLU; kSwiglu H = silu(gate)·up stored as BF16/FP32;
 // kSwigluFp8 H quantised to FP8 for the down projection: each row's 128 columns of a tile (one 1x128
-// group) get the scale s = amax/448 (1 where amax = 0) and the codes e4m3_rne(clamp(h / s, ±448)).
+// group) get the codes e4m3_rne(clamp(h · (448/amax), ±448)) and the dequantisation scale amax/448
+// (factor and scale 1 where amax = 0).
 // D then points to the codes [G·M_max, I] (bytes) and workspace to the scales [G][I/128][ldsa]
-// (the MN-major LHS scale layout of the masked GEMM). A separate instantiation, because the
-// correctly rounded divisions raise the epilogue's register pressure.
+// (the MN-major LHS scale layout of the masked GEMM). A separate instantiation: holding a row's 128
+// H values until their amax is known raises the epilogue's register pressure.
 constexpr int kSwiglu = 1;
 constexpr int kSwigluFp8 = 2;
 // Bits 8..31 of the flags word hold the time limit of the pipeline waits in microseconds
@@ -978,6 +979,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
           float amax = 0.0f;
 #pragma unroll
           for (int j = 0; j < 128; ++j) amax = fmaxf(amax, fabsf(acc[j]));
+          // one division per row for the factor and one for the scale; a product per element
+          const float f = amax > 0.0f ? __fdiv_rn(448.0f, amax) : 1.0f;
           const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
           uint8_t* qrow = reinterpret_cast<uint8_t*>(p.D) + (size_t)(tile.a_row + row_in_tile) * p.swiglu_i + h_col0;
 #pragma unroll
@@ -986,8 +989,8 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int c = j + q * 4;
-              const uint32_t lo = e4m3x2_satfinite(__fdiv_rn(acc[c], sc), __fdiv_rn(acc[c + 1], sc));
-              const uint32_t hi = e4m3x2_satfinite(__fdiv_rn(acc[c + 2], sc), __fdiv_rn(acc[c + 3], sc));
+              const uint32_t lo = e4m3x2_satfinite(__fmul_rn(acc[c], f), __fmul_rn(acc[c + 1], f));
+              const uint32_t hi = e4m3x2_satfinite(__fmul_rn(acc[c + 2], f), __fmul_rn(acc[c + 3], f));
               w[q] = lo | (hi << 16);
             }
             *reinterpret_cast<uint4*>(qrow + j) = make_uint4(w[0], w[1], w[2], w[3]);

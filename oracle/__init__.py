@@ -202,17 +202,22 @@ def e4m3_encode_rne(y) -> np.ndarray:
 
 
 def quantize_rows_e4m3(H, group: int = 128):
-    """FP8 cast of H [..., R, C] per 1 x ``group`` group of each row: s = amax/448 in FP32 (1 where
-    amax = 0), codes = e4m3_rne(clamp(H / s, ±448)) with the FP32 division. Returns (codes [..., R, C]
-    uint8, scales [..., C/group, R] float32: the MN-major LHS scale layout, unpadded)."""
+    """FP8 cast of H [..., R, C] per 1 x ``group`` group of each row: the group is mapped onto the
+    E4M3 range by the factor 448/amax (an FP32 division, once per group) and its dequantisation scale
+    is s = amax/448 (FP32); codes = e4m3_rne(clamp(H · (448/amax), ±448)) with the FP32 product. An
+    all-zero group has factor 1 and scale 1. Returns (codes [..., R, C] uint8, scales [..., C/group, R]
+    float32: the MN-major LHS scale layout, unpadded)."""
     H = np.asarray(H, np.float32)
     *lead, R, C = H.shape
     if C % group:
         raise ValueError("the row length must be a multiple of the group")
     Hg = H.reshape(*lead, R, C // group, group)
     amax = np.max(np.abs(Hg), axis=-1)                                     # [..., R, C/group] FP32
-    s = np.where(amax > 0, (amax / np.float32(448.0)).astype(np.float32), np.float32(1.0)).astype(np.float32)
-    y = (Hg / s[..., None]).astype(np.float32)                            # FP32 (IEEE) division
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
+    s = np.where(nz, (safe / np.float32(448.0)).astype(np.float32), np.float32(1.0)).astype(np.float32)
+    inv = np.where(nz, (np.float32(448.0) / safe).astype(np.float32), np.float32(1.0)).astype(np.float32)
+    y = (Hg * inv[..., None]).astype(np.float32)                          # FP32 product, rounded once
     y = np.clip(y, np.float32(-448.0), np.float32(448.0))
     codes = e4m3_encode_rne(y).reshape(*lead, R, C)
     return codes, np.swapaxes(s, -1, -2).copy()
