@@ -462,7 +462,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   if (!swiglu) fit_cluster_splits(cfg, mode, K, block_scaled, out_f32);
   const int d_cols = swiglu ? N / 2 : N;   // width of D (fused SwiGLU: H has I = N/2 columns)
   if (swiglu) {
-    // one tile = 128 gate rows + 128 up rows of B; no split-K
+    // one tile = 128 gate rows + 128 up rows of B; no host split-K (the tail split may still apply)
     cfg.block_n = 256;
     cfg.stages = block_scaled ? dg::BsSmemPlan::kStages : dg::stages_for(256);
     cfg.splits = 1;
@@ -492,9 +492,10 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles;   // masked: counted on the device
   p.raster_m = (int16_t)cfg.raster_m;
-  // Tail split (no host split-K, not the fused SwiGLU): the workspace holds at most one wave of
-  // split units, the counters one per CTA.
-  const bool tail = !swiglu && cfg.splits == 1 && tail_splits_setting() > 1;
+  // Tail split (no host split-K; the fused SwiGLU on the FP32-scale kernel, whose split-K step
+  // reduces the gate and up partials before the hand-over, but not on the block-scaled one): the
+  // workspace holds at most one wave of split units, the counters one per CTA.
+  const bool tail = !(swiglu && block_scaled) && cfg.splits == 1 && tail_splits_setting() > 1;
   p.tail_splits = (int16_t)(tail ? tail_splits_setting() : 1);
   // (the block-scaled kernel reads these as its packed UE8M0 words)
   p.sA = static_cast<const float*>(sA);
@@ -503,7 +504,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.masked_m = mode == dg::kMasked ? idx : nullptr;
   p.D = D;
   p.status = st->status;
-  if (quant_h) p.workspace = h_scales;   // (the fused SwiGLU has no split-K workspace)
+  if (quant_h) p.h_scales = h_scales;   // (masked: no m_indices)
   if (accumulate && static_cast<const void*>(C) != D) {
     cudaError_t ce = cudaMemcpyAsync(D, C, (size_t)rows * N * sizeof(float), cudaMemcpyDeviceToDevice, stream);
     if (ce != cudaSuccess) return fail_cuda(ce, "cudaMemcpyAsync(C -> D)");

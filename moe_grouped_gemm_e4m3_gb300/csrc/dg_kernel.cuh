@@ -69,7 +69,10 @@ struct GemmParams {
   int16_t tail_splits;  // most K ranges a tile of a last, partial wave may be cut into (1: never)
   const float* sA;           // block-scaled kernel: the packed UE8M0 words (uint32) instead
   const float* sB;           // block-scaled kernel: the packed UE8M0 words (uint32) instead
-  const int32_t* m_indices;  // K-grouped: the [G+1] K offsets of the groups (K is then K_total)
+  union {
+    const int32_t* m_indices;  // K-grouped: the [G+1] K offsets of the groups (K is then K_total)
+    float* h_scales;           // fused SwiGLU with FP8 H (masked): the scales of H, [G][I/128][ldsa]
+  };
   const int32_t* masked_m;
   void* D;           // row-major, row stride N elements (used by predicated stores)
   float* workspace;  // split-K partial tiles
@@ -97,7 +100,7 @@ constexpr int kFlagPairB = 0x10;
 // kSwigluFp8 H quantised to FP8 for the down projection: each row's 128 columns of a tile (one 1x128
 // group) get the codes e4m3_rne(clamp(h · (448/amax), ±448)) and the dequantisation scale amax/448
 // (factor and scale 1 where amax = 0).
-// D then points to the codes [G·M_max, I] (bytes) and workspace to the scales [G][I/128][ldsa]
+// D then points to the codes [G·M_max, I] (bytes) and h_scales to the scales [G][I/128][ldsa]
 // (the MN-major LHS scale layout of the masked GEMM). A separate instantiation: holding a row's 128
 // H values until their amax is known raises the epilogue's register pressure.
 constexpr int kSwiglu = 1;
@@ -995,7 +998,7 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
             }
             *reinterpret_cast<uint4*>(qrow + j) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          p.workspace[((size_t)tile.g * (p.swiglu_i / 128) + tile.n_blk) * p.ldsa + m_local] = sc;
+          p.h_scales[((size_t)tile.g * (p.swiglu_i / 128) + tile.n_blk) * p.ldsa + m_local] = sc;
         }
         continue;
       }
