@@ -492,10 +492,10 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   p.kb_per_split = cfg.kb_per_split;
   p.num_tiles = mode == dg::kMasked ? 0 : cfg.tiles;   // masked: counted on the device
   p.raster_m = (int16_t)cfg.raster_m;
-  // Tail split (no host split-K; the fused SwiGLU on the FP32-scale kernel, whose split-K step
-  // reduces the gate and up partials before the hand-over, but not on the block-scaled one): the
-  // workspace holds at most one wave of split units, the counters one per CTA.
-  const bool tail = !(swiglu && block_scaled) && cfg.splits == 1 && tail_splits_setting() > 1;
+  // Tail split (no host split-K; the fused SwiGLU included: its split-K step reduces the gate and
+  // up partials before H is formed): the workspace holds at most one wave of split units, the
+  // counters one per CTA.
+  const bool tail = cfg.splits == 1 && tail_splits_setting() > 1;
   p.tail_splits = (int16_t)(tail ? tail_splits_setting() : 1);
   // (the block-scaled kernel reads these as its packed UE8M0 words)
   p.sA = static_cast<const float*>(sA);

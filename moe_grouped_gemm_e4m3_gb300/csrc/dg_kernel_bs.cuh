@@ -447,66 +447,6 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
       const int n_col0 = tile.n_blk * BN + cgrp * EPI_COLS;
       const bool col_exists = n_col0 < p.N;
 
-      if constexpr (SWIGLU) {
-        // H = silu(gate)·up for this warp's 64 of the tile's 128 columns of H (row stride I)
-        if (!active || !__any_sync(0xffffffffu, row_exists)) continue;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) acc[j] = silu_f32(acc[j]) * acc[64 + j];
-        const int h_col0 = tile.n_blk * 128 + cgrp * 64;
-        if (__all_sync(0xffffffffu, row_exists)) {
-          constexpr int kColsPerBox = OUT_F32 ? 16 : 32;
-#pragma unroll
-          for (int chunk = 0; chunk < 64 / kColsPerBox; ++chunk) {
-            const uint32_t sel = store_count & 1;
-            if (store_count >= 2) {
-              if (lane == 0) tma_store_wait_read_1();
-              __syncwarp();
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t w0, w1, w2, w3;
-              if constexpr (OUT_F32) {
-                const int c = chunk * 16 + j * 4;
-                w0 = accu[c]; w1 = accu[c + 1]; w2 = accu[c + 2]; w3 = accu[c + 3];
-              } else {
-                const int c = chunk * 32 + j * 8;
-                w0 = pack_bf16x2(acc[c], acc[c + 1]); w1 = pack_bf16x2(acc[c + 2], acc[c + 3]);
-                w2 = pack_bf16x2(acc[c + 4], acc[c + 5]); w3 = pack_bf16x2(acc[c + 6], acc[c + 7]);
-              }
-              const uint32_t phys = (uint32_t)(j ^ ((lane >> 1) & 3));
-              st_shared_v4(staging_addr + sel * Plan::kStagingBox + lane * 64 + phys * 16, w0, w1, w2, w3);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmD, staging + sel * Plan::kStagingBox, h_col0 + chunk * kColsPerBox, tile.a_row + quad * 32);
-              tma_store_commit();
-            }
-            ++store_count;
-            __syncwarp();
-          }
-        } else if (row_exists) {
-          // predicated plain stores: rows past masked_m stay untouched
-          const size_t hrow = (size_t)(tile.a_row + row_in_tile) * p.swiglu_i + h_col0;
-          if constexpr (OUT_F32) {
-            float* dst = reinterpret_cast<float*>(p.D) + hrow;
-#pragma unroll
-            for (int j = 0; j < 64; j += 4)
-              *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-          } else {
-            uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + hrow;
-#pragma unroll
-            for (int j = 0; j < 64; j += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(acc[j], acc[j + 1]); v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-              v.z = pack_bf16x2(acc[j + 4], acc[j + 5]); v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-              *reinterpret_cast<uint4*>(dst + j) = v;
-            }
-          }
-        }
-        continue;
-      }
-
       if (kClusterCapable && (p.flags & kFlagClusterSplit)) {
         // one unit per CTA: the partial goes to this CTA's stage buffers (idle once the MMA is
         // done) and the reduction follows the loop. Rows or columns outside the tile (a warp that
@@ -567,6 +507,68 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
             }
           }
         }
+      }
+
+      // (fused SwiGLU: the split-K step above publishes and reduces each warp's 64 gate and 64 up
+      // columns under its own 128 slots of the partial tile, so the last split holds both)
+      if constexpr (SWIGLU) {
+        // H = silu(gate)·up for this warp's 64 of the tile's 128 columns of H (row stride I)
+        if (!active || !__any_sync(0xffffffffu, row_exists)) continue;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = silu_f32(acc[j]) * acc[64 + j];
+        const int h_col0 = tile.n_blk * 128 + cgrp * 64;
+        if (__all_sync(0xffffffffu, row_exists)) {
+          constexpr int kColsPerBox = OUT_F32 ? 16 : 32;
+#pragma unroll
+          for (int chunk = 0; chunk < 64 / kColsPerBox; ++chunk) {
+            const uint32_t sel = store_count & 1;
+            if (store_count >= 2) {
+              if (lane == 0) tma_store_wait_read_1();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t w0, w1, w2, w3;
+              if constexpr (OUT_F32) {
+                const int c = chunk * 16 + j * 4;
+                w0 = accu[c]; w1 = accu[c + 1]; w2 = accu[c + 2]; w3 = accu[c + 3];
+              } else {
+                const int c = chunk * 32 + j * 8;
+                w0 = pack_bf16x2(acc[c], acc[c + 1]); w1 = pack_bf16x2(acc[c + 2], acc[c + 3]);
+                w2 = pack_bf16x2(acc[c + 4], acc[c + 5]); w3 = pack_bf16x2(acc[c + 6], acc[c + 7]);
+              }
+              const uint32_t phys = (uint32_t)(j ^ ((lane >> 1) & 3));
+              st_shared_v4(staging_addr + sel * Plan::kStagingBox + lane * 64 + phys * 16, w0, w1, w2, w3);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, staging + sel * Plan::kStagingBox, h_col0 + chunk * kColsPerBox, tile.a_row + quad * 32);
+              tma_store_commit();
+            }
+            ++store_count;
+            __syncwarp();
+          }
+        } else if (row_exists) {
+          // predicated plain stores: rows past masked_m stay untouched
+          const size_t hrow = (size_t)(tile.a_row + row_in_tile) * p.swiglu_i + h_col0;
+          if constexpr (OUT_F32) {
+            float* dst = reinterpret_cast<float*>(p.D) + hrow;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4)
+              *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+          } else {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + hrow;
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(acc[j], acc[j + 1]); v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+              v.z = pack_bf16x2(acc[j + 4], acc[j + 5]); v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+              *reinterpret_cast<uint4*>(dst + j) = v;
+            }
+          }
+        }
+        continue;
       }
 
       // ---------------- output
