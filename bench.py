@@ -726,7 +726,8 @@ def run_reference(args, rank, world):
 
 def run_all_configs(args):
     """One JSON line per shape of every workload configuration: time (CUDA events, mean over reps,
-    L2 flushed before each), TFLOP/s, the binding roof and the fraction of it."""
+    L2 flushed before each, with the median beside it), TFLOP/s, the binding roof and the fraction
+    of it."""
     import torch
     import dg_inputs
     import moe_grouped_gemm_e4m3_gb300 as dg
@@ -748,14 +749,18 @@ def run_all_configs(args):
             e1.record()
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1))
+        medians.append(float(np.median(ts)))
         return float(np.mean(ts))
+
+    medians = []   # the median of each timeit call, reported beside the mean (a rep can be an outlier)
 
     def report(config, shape, flops, nbytes, ms, extra=None):
         t_tc, t_hbm = flops / (fp8_peak * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9)
         bound = "tensor" if t_tc >= t_hbm else "hbm"
         frac = (flops / (ms * 1e-3) / 1e12 / fp8_peak) if bound == "tensor" else (nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"])
         line = {"config": config, "shape": shape, "us": round(ms * 1e3, 2), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
-                "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": bound, "roof_frac": round(frac, 3)}
+                "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": bound, "roof_frac": round(frac, 3),
+                "us_median": round(medians[-1] * 1e3, 2) if medians else None}
         line.update(extra or {})
         print(json.dumps(line), flush=True)
 
