@@ -128,6 +128,34 @@ def test_timeout_masked_swiglu(dg):
     _timeout_then_recover(dg, lambda: dg.dg_fp8_grouped_masked_swiglu(A, sA, B, sB, MM, H), H)
 
 
+def test_timeout_masked_swiglu_fp8(dg):
+    # H cast to FP8: the codes (Hq) and the scales (sH) both come back unchanged after a timeout
+    G, M_max, N2, K = 8, 192, 1024, 1024
+    mm = dg_inputs.make_masked_m(G, M_max, seed=8)
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=8)
+    b = dg_inputs.make_b(G, N2, K, seed=8)
+    A, sA, B, sB, MM = dev(a.A), dev(a.sA), dev(b.B), dev(b.sB), dev(mm)
+    Hq = torch.full((G, M_max, N2 // 2), 0xFF, dtype=torch.uint8, device="cuda")
+    sH = torch.full((G, N2 // 2 // 128, M_max), float("nan"), dtype=torch.float32, device="cuda")
+    call = lambda: dg.dg_fp8_grouped_masked_swiglu_fp8(A, sA, B, sB, MM, Hq, sH)
+    call()
+    torch.cuda.synchronize()
+    ref_s = sH.clone()
+    _timeout_then_recover(dg, call, Hq)
+    assert torch.equal(sH.view(torch.int32), ref_s.view(torch.int32)), "the scales after a timeout differ"
+
+
+def test_timeout_masked_swiglu_ue8m0(dg):
+    G, M_max, N2, K = 8, 192, 1024, 1024
+    mm = dg_inputs.make_masked_m(G, M_max, seed=9)
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=9, ue8m0=True)
+    b = dg_inputs.make_b(G, N2, K, seed=9, ue8m0=True)
+    A, B, MM = dev(a.A), dev(b.B), dev(mm)
+    sA, sB = dev(dg_inputs.pack_ue8m0_a(a.sA)), dev(dg_inputs.pack_ue8m0_b(b.sB))
+    H = bf16_sentinel((G, M_max, N2 // 2))
+    _timeout_then_recover(dg, lambda: dg.dg_fp8_grouped_masked_swiglu_ue8m0(A, sA, B, sB, MM, H), H)
+
+
 def test_timeout_k_grouped(dg):
     M, N, off = 512, 1024, np.array([0, 1024, 1024, 3072], np.int32)
     K = int(off[-1])
