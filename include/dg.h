@@ -255,7 +255,9 @@ dg_status dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32(const uint8_t* A, const 
  *      H[g,m,j] = silu(D[g,m,j]) · D[g,m,I+j],  D = the masked GEMM,  silu(x) = x / (1 + e^-x)
  *      (SwiGLU as defined by Shazeer, "GLU Variants Improve Transformer", 2020)
  *   Rows m >= masked_m[g] of H are never written. The FP32-scale kernel computes D in FP32 and H in FP32
- *   (expf), then rounds H to BF16 once: H_bf16 == RNE(H_f32).
+ *   (silu with the fast exponential and division, relative error ~1e-6), then rounds H to BF16 once:
+ *   H_bf16 == RNE(H_f32). Like the masked GEMM it may cut the tiles of a last, partial wave along K
+ *   (dg_set_tail_splits), using the library's workspace.
  */
 dg_status dg_fp8_grouped_masked_swiglu(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                                        const int32_t* masked_m, uint16_t* H, int G, int M_max, int N, int K,
@@ -358,9 +360,10 @@ int dg_get_num_sms(void);
    detection. */
 long long dg_set_wait_limit_us(long long us);
 
-/* Tail split of the dense, contiguous and masked forms (dg_fp8_gemm_nt_noalloc included), with
-   either scale form (not the fused SwiGLU or the K-grouped form; calls whose configuration already
-   splits K are unaffected). When the output tiles of a launch
+/* Tail split of the dense, contiguous and masked forms (dg_fp8_gemm_nt_noalloc and the fused
+   SwiGLU included), with either scale form (not the K-grouped form; calls whose configuration
+   already splits K are unaffected). The fused SwiGLU reduces the gate and up partials before it
+   forms H. When the output tiles of a launch
    leave a last, partial wave of at most half the grid, the kernel may cut each of those tiles into
    up to n K ranges, computed by otherwise idle SMs and summed in range order (deterministic) by the
    last range to finish, exactly as split-K does. The kernel takes the split only when its cost model
