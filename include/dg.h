@@ -395,6 +395,22 @@ int dg_set_tail_splits(int n);
    implementation's choice. */
 int dg_set_pair_b(int on);
 
+/* Programmatic dependent launch for every GEMM call. With on != 0, each kernel is launched with
+   programmatic stream serialization: it may start while the kernel ahead of it in the stream is
+   still running, set up its shared memory, barriers and tensor memory, and then wait
+   (griddepcontrol.wait) until that kernel has completed and its writes are visible, before it
+   reads any input. Each kernel also signals, once its own setup is done, that the next kernel may
+   start (griddepcontrol.launch_dependents). Back-to-back calls on one stream then hide part of
+   each launch's setup. A kernel that follows one of these in the stream starts early only if it
+   was itself launched for it. Results are the same bits either way. on = 0 (the default; the
+   environment variable DG_PDL=1 sets the initial value to on) launches in plain stream order.
+   Returns the previous value (0 or 1). The pages name a PDL switch among the library's utilities,
+   set_pdl / get_pdl ("DeepGEMM: İnce ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri",
+   tr.news.hada.io/topic?id=19459, § "Yardımcı fonksiyonlar ve ortam değişkenleri"). */
+int dg_set_pdl(int on);
+/* The current setting of dg_set_pdl (0 or 1). */
+int dg_get_pdl(void);
+
 /* Split-K inside thread-block clusters (dense and contiguous forms, either scale form). When a call
    splits K (few output tiles) into at most 8 ranges and every tile's ranges fit on the GPU at once
    as one cluster of CTAs, the ranges reduce through distributed shared memory: partials in each

@@ -37,7 +37,8 @@ __all__ = [
     "dg_fp8_grouped_contiguous_f32", "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_fp8_gemm_nt_noalloc",
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms",
     "dg_get_num_sms", "dg_get_device_status", "dg_last_error_string", "dg_query_config",
-    "dg_set_tail_splits", "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
+    "dg_set_tail_splits", "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_set_pdl", "dg_get_pdl",
+    "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_fp8",
@@ -60,7 +61,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_grouped_masked", "dg_fp8_grouped_masked_f32", "dg_get_tma_aligned_size",
     "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms", "dg_get_num_sms", "dg_get_device_status",
     "dg_last_error_string", "dg_query_config", "dg_fp8_gemm_nt_noalloc", "dg_set_tail_splits",
-    "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b",
+    "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_set_pdl", "dg_get_pdl",
     "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
@@ -120,6 +121,8 @@ def load(build_if_missing: bool = True):
     lib.dg_set_tail_splits.restype, lib.dg_set_tail_splits.argtypes = i32, [i32]
     lib.dg_set_cluster_split.restype, lib.dg_set_cluster_split.argtypes = i32, [i32]
     lib.dg_set_pair_b.restype, lib.dg_set_pair_b.argtypes = i32, [i32]
+    lib.dg_set_pdl.restype, lib.dg_set_pdl.argtypes = i32, [i32]
+    lib.dg_get_pdl.restype, lib.dg_get_pdl.argtypes = i32, []
     lib.dg_set_wait_limit_us.restype, lib.dg_set_wait_limit_us.argtypes = ctypes.c_longlong, [ctypes.c_longlong]
     lib.dg_get_device_status.restype, lib.dg_get_device_status.argtypes = i32, [ctypes.POINTER(i32), P]
     lib.dg_last_error_string.restype, lib.dg_last_error_string.argtypes = ctypes.c_char_p, []
@@ -570,6 +573,17 @@ def dg_set_pair_b(on: bool) -> bool:
     """Allow or forbid (default) pairs of CTAs that share B tiles through TMA multicast. Returns the
     previous value; results are bit-identical either way."""
     return bool(load().dg_set_pair_b(1 if on else 0))
+
+
+def dg_set_pdl(on: bool) -> bool:
+    """Launch every GEMM with programmatic dependent launch (it may start before the previous kernel
+    in the stream ends, and waits for that kernel's results before reading its inputs), or not (the
+    default). Returns the previous value; results are bit-identical either way."""
+    return bool(load().dg_set_pdl(1 if on else 0))
+
+
+def dg_get_pdl() -> bool:
+    return bool(load().dg_get_pdl())
 
 
 def dg_set_tail_splits(n: int) -> int:

@@ -63,6 +63,19 @@ bool cluster_split_setting() {
 // no split-K): off unless DG_PAIR_B=1 or dg_set_pair_b(1). Measured on GB300, the FP32-scale kernel
 // is bound by its per-K-block TMEM round trip, not by the L2 feed that pairing relieves, and paired
 // launches lose the tail split: 4096x7168x16384 397 us single, 419 us paired.
+// Programmatic dependent launch: off unless DG_PDL=1 or dg_set_pdl(1).
+std::atomic<int> g_pdl{-1};
+bool pdl_setting() {
+  int v = g_pdl.load();
+  if (v < 0) {
+    const char* e = std::getenv("DG_PDL");
+    int expected = -1;
+    g_pdl.compare_exchange_strong(expected, (e && std::atoi(e) != 0) ? 1 : 0);
+    v = g_pdl.load();
+  }
+  return v != 0;
+}
+
 std::atomic<int> g_pair_b{-1};
 bool pair_b_setting() {
   int v = g_pair_b.load();
@@ -589,6 +602,7 @@ dg_status run_gemm(int mode, bool out_f32, const uint8_t* A, const void* sA, con
   a.out_f32 = out_f32;
   a.grid = cfg.grid;
   a.stream = stream;
+  a.pdl = pdl_setting();
   if (print_configs()) {
     static const char* names[3] = {"dense", "contiguous", "masked"};
     std::fprintf(stderr, "[dg] %s%s%s%s rows=%d N=%d K=%d G=%d: BM=128 BN=%d stages=%d splits=%d%s grid=%d tiles=%d\n",
@@ -690,6 +704,7 @@ dg_status run_k_grouped(bool out_f32, const uint8_t* A, const void* sA, const ui
   a.out_f32 = out_f32;
   a.grid = tiles < sms ? tiles : sms;
   a.stream = stream;
+  a.pdl = pdl_setting();
   if (print_configs())
     std::fprintf(stderr, "[dg] k-grouped%s%s G=%d M=%d N=%d K_total=%d: BM=128 BN=%d grid=%d tiles=%d\n",
                  block_scaled ? "/ue8m0" : "", out_f32 ? "/f32" : "", G, M, N, K_total, bn, a.grid, tiles);
@@ -938,6 +953,14 @@ int dg_set_pair_b(int on) {
   g_pair_b.store(on ? 1 : 0);
   return prev;
 }
+
+int dg_set_pdl(int on) {
+  const int prev = pdl_setting() ? 1 : 0;
+  g_pdl.store(on ? 1 : 0);
+  return prev;
+}
+
+int dg_get_pdl(void) { return pdl_setting() ? 1 : 0; }
 
 int dg_set_cluster_split(int on) {
   const int prev = cluster_split_setting() ? 1 : 0;

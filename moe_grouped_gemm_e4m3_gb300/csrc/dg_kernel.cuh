@@ -488,6 +488,18 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
     *no_partial = 0;
     fence_barrier_init();
   }
+  if (warp == R::kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == R::kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  // Programmatic dependent launch: everything above reads no global memory that the previous
+  // kernel in the stream may still be writing; everything below may.
+  griddep_wait();
   if (warp == 0) {
     // the launch's work units, the same in every CTA (masked: tiles counted from masked_m)
     int tiles = p.num_tiles;
@@ -501,17 +513,9 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
       st[8] = sc.whole; st[9] = sc.splits; st[10] = sc.kps; st[11] = sc.units;
     }
   }
-  if (warp == R::kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmD);
-  }
-  if (warp == R::kMmaWarp) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   // pair mode: the peer's multicast copies and MMA commits arrive on this CTA's barriers, so both
   // CTAs' barriers are initialised before either starts
   if (pair) cluster_sync_all();

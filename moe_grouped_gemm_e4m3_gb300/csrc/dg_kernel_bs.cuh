@@ -159,6 +159,10 @@ __global__ void __launch_bounds__(BsRoles::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // Programmatic dependent launch: the setup above reads no global memory that the previous kernel
+  // in the stream may still be writing; the roles below do.
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 

@@ -17,6 +17,7 @@ struct LaunchArgs {
   bool out_f32;
   int grid;
   int cluster;   // > 1: launch as clusters of this many CTAs (cluster split-K)
+  bool pdl;      // programmatic dependent launch (dg_set_pdl): may start before the previous kernel ends
   cudaStream_t stream;
 };
 
@@ -51,21 +52,32 @@ int cluster_capacity_contiguous(int block_n, bool out_f32, int cluster);
 // The same for the block-scaled kernel (dense or contiguous).
 int cluster_capacity_bs(Mode mode, bool out_f32, int cluster);
 
-// Launches `kernel` as clusters of `cluster` CTAs (1-D grid of `grid` CTAs).
+// Launches `kernel` on a 1-D grid of `grid` CTAs: as clusters of `cluster` CTAs when cluster > 1,
+// and with programmatic stream serialization when pdl is set (the kernels wait for the previous
+// kernel's results with griddepcontrol.wait before their first global read).
 template <typename Kernel>
-cudaError_t launch_clustered(Kernel kernel, const LaunchArgs& a, int threads, size_t smem_bytes) {
+cudaError_t launch_kernel(Kernel kernel, const LaunchArgs& a, int threads, size_t smem_bytes) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = a.stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = (unsigned)a.cluster;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (a.cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)a.cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (a.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, a.tmA, a.tmB, a.tmD, a.p);
 }
 
@@ -114,9 +126,7 @@ cudaError_t launch_instance(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  if (a.cluster > 1) return launch_clustered(kernel, a, R::kThreads, Plan::kDynamicBytes);
-  kernel<<<a.grid, R::kThreads, Plan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
-  return cudaGetLastError();
+  return launch_kernel(kernel, a, R::kThreads, Plan::kDynamicBytes);
 }
 
 // Resident clusters of `cluster` CTAs for one instantiation (an occupancy query; nothing runs).
@@ -151,9 +161,7 @@ cudaError_t launch_bs_instance(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  if (a.cluster > 1) return launch_clustered(kernel, a, BsRoles::kThreads, BsSmemPlan::kDynamicBytes);
-  kernel<<<a.grid, BsRoles::kThreads, BsSmemPlan::kDynamicBytes, a.stream>>>(a.tmA, a.tmB, a.tmD, a.p);
-  return cudaGetLastError();
+  return launch_kernel(kernel, a, BsRoles::kThreads, BsSmemPlan::kDynamicBytes);
 }
 
 template <Mode MODE>

@@ -187,6 +187,19 @@ __device__ __forceinline__ float4 cluster_sum_v4(uint32_t addr, int S) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization may start
+// before the kernel ahead of it in the stream has finished; griddep_wait() then blocks until that
+// kernel has completed and its memory operations are visible. Without the launch attribute both
+// instructions do nothing.
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream (if launched for it) begin its own launch while this one runs.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
 // TMA (tensor maps are __grid_constant__ kernel parameters)
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
