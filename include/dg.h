@@ -70,6 +70,7 @@ typedef enum {
 #define DG_DEV_BAD_GROUP_INDEX 0x1  /* contiguous: m_indices[m] >= G or < -1, or two groups in one 128-row block */
 #define DG_DEV_BAD_MASKED_M 0x2     /* masked: masked_m[g] < 0 or > M_max (clamped) */
 #define DG_DEV_TIMEOUT 0x4          /* a pipeline wait exceeded its time limit; the kernel abandoned the work */
+#define DG_DEV_BAD_SCALE 0x8        /* dg_transform_sf_into_ue8m0_*: a scale was not a power of two in [2^-127, 2^127] */
 
 typedef void* dg_stream_t; /* cudaStream_t */
 
@@ -394,6 +395,24 @@ int dg_set_tail_splits(int n);
    7minutos.es, § "Detalles y beneficios técnicos"); sharing them through multicast is this
    implementation's choice. */
 int dg_set_pair_b(int on);
+
+/* Scale factors into the packed UE8M0 layout of the block-scaled (_ue8m0) calls, on the GPU: the
+   counterpart of the library's helper that brings scaling factors into the layout its SM100 kernels
+   require ("DeepGEMM: İnce ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri",
+   tr.news.hada.io/topic?id=19459, § "Yardımcı fonksiyonlar ve ortam değişkenleri" and § "GEMM
+   arayüzü ve yerleşim kısıtları": four UE8M0 codes per int32).
+     _a: sA [G][ceil(K/128)][align4(M)] FP32 (A's MN-major layout; G = 1 for the dense and contiguous
+         calls, M = M_max for the masked ones) -> sA_packed [G][ceil(ceil(K/128)/4)][align4(M)] int32.
+     _b: sB [G][ceil(N/128)][ceil(K/128)] FP32 -> sB_packed [G][ceil(N/128)][ceil(ceil(K/128)/4)] int32.
+   Byte j of each word is the code of K-block 4q + j (bytes past the last K-block: 127). A scale
+   2^e with e in [-127, 127] becomes the code e + 127, so the packed call computes exactly what the
+   FP32-scale call computes with these scales. A zero scale (the padding rows m >= M of A's layout)
+   packs as 127. Any other value sets DG_DEV_BAD_SCALE in the device status word and packs as the
+   smallest power of two at or above its magnitude (clamped to [2^-127, 2^127]; NaN as 1): the
+   block-scaled MMA cannot apply it exactly. Device pointers, 4-byte aligned, launched on `stream`;
+   the output must not overlap the input. */
+dg_status dg_transform_sf_into_ue8m0_a(const float* sA, int32_t* sA_packed, int G, int M, int K, dg_stream_t stream);
+dg_status dg_transform_sf_into_ue8m0_b(const float* sB, int32_t* sB_packed, int G, int N, int K, dg_stream_t stream);
 
 /* Programmatic dependent launch for every GEMM call. With on != 0, each kernel is launched with
    programmatic stream serialization: it may start while the kernel ahead of it in the stream is

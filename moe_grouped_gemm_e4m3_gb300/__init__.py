@@ -38,7 +38,7 @@ __all__ = [
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms",
     "dg_get_num_sms", "dg_get_device_status", "dg_last_error_string", "dg_query_config",
     "dg_set_tail_splits", "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_set_pdl", "dg_get_pdl",
-    "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
+    "dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b", "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_fp8",
@@ -49,11 +49,11 @@ __all__ = [
     "dg_fp8_k_grouped_gemm_tn_contiguous", "dg_fp8_k_grouped_gemm_tn_contiguous_f32",
     "dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0", "dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32", "EXPORTED_SYMBOLS", "DG_OK", "DG_ERR_INVALID_ARG", "DG_ERR_ALIGNMENT", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_DEVICE_STATUS", "DG_DEV_BAD_GROUP_INDEX", "DG_DEV_BAD_MASKED_M",
-    "DG_DEV_TIMEOUT",
+    "DG_DEV_TIMEOUT", "DG_DEV_BAD_SCALE",
 ]
 
 DG_OK, DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_DEVICE_STATUS = range(6)
-DG_DEV_BAD_GROUP_INDEX, DG_DEV_BAD_MASKED_M, DG_DEV_TIMEOUT = 0x1, 0x2, 0x4
+DG_DEV_BAD_GROUP_INDEX, DG_DEV_BAD_MASKED_M, DG_DEV_TIMEOUT, DG_DEV_BAD_SCALE = 0x1, 0x2, 0x4, 0x8
 
 # Every symbol include/dg.h declares (checked against the built library by the CPU tests).
 EXPORTED_SYMBOLS = (
@@ -62,7 +62,7 @@ EXPORTED_SYMBOLS = (
     "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms", "dg_get_num_sms", "dg_get_device_status",
     "dg_last_error_string", "dg_query_config", "dg_fp8_gemm_nt_noalloc", "dg_set_tail_splits",
     "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_set_pdl", "dg_get_pdl",
-    "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
+    "dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b", "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_fp8",
@@ -123,6 +123,9 @@ def load(build_if_missing: bool = True):
     lib.dg_set_pair_b.restype, lib.dg_set_pair_b.argtypes = i32, [i32]
     lib.dg_set_pdl.restype, lib.dg_set_pdl.argtypes = i32, [i32]
     lib.dg_get_pdl.restype, lib.dg_get_pdl.argtypes = i32, []
+    for name in ("dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i32, [P, P, i32, i32, i32, P]
     lib.dg_set_wait_limit_us.restype, lib.dg_set_wait_limit_us.argtypes = ctypes.c_longlong, [ctypes.c_longlong]
     lib.dg_get_device_status.restype, lib.dg_get_device_status.argtypes = i32, [ctypes.POINTER(i32), P]
     lib.dg_last_error_string.restype, lib.dg_last_error_string.argtypes = ctypes.c_char_p, []
@@ -514,6 +517,38 @@ def dg_fp8_grouped_masked_swiglu_ue8m0(A, sA, B, sB, masked_m, H, stream=None):
 
 def dg_fp8_grouped_masked_swiglu_ue8m0_f32(A, sA, B, sB, masked_m, H, stream=None):
     return _masked("dg_fp8_grouped_masked_swiglu_ue8m0_f32", True, A, sA, B, sB, masked_m, H, stream)
+
+
+def dg_transform_sf_into_ue8m0_a(sA, sA_packed, M, K, stream=None):
+    """A's FP32 scales sA [ceil(K/128), align4(M)] (or [G, ...]; powers of two, zero for padding rows)
+    -> packed UE8M0 words sA_packed [ceil(ceil(K/128)/4), align4(M)] (or [G, ...]) int32, on the GPU.
+    A value that is not a power of two sets DG_DEV_BAD_SCALE (dg_get_device_status)."""
+    import torch
+    s = _shape(sA, "sA")
+    if len(s) not in (2, 3):
+        raise ValueError(f"sA must be [ceil(K/128), align4(M)] or [G, ceil(K/128), align4(M)], got {list(s)}")
+    G = s[0] if len(s) == 3 else 1
+    nkb, ldsa = -(-K // 128), dg_get_tma_aligned_size(M, 4)
+    _expect(sA, "sA", s[:-2] + (nkb, ldsa))
+    _expect(sA_packed, "sA_packed", s[:-2] + (-(-nkb // 4), ldsa))
+    _check(load().dg_transform_sf_into_ue8m0_a(_ptr(sA, "sA", (torch.float32,)),
+                                               _ptr(sA_packed, "sA_packed", (torch.int32,)), G, M, K, _stream(stream)))
+
+
+def dg_transform_sf_into_ue8m0_b(sB, sB_packed, N, K, stream=None):
+    """B's FP32 scales sB [ceil(N/128), ceil(K/128)] (or [G, ...]; powers of two) -> packed UE8M0 words
+    sB_packed [ceil(N/128), ceil(ceil(K/128)/4)] (or [G, ...]) int32, on the GPU. A value that is not a
+    power of two sets DG_DEV_BAD_SCALE (dg_get_device_status)."""
+    import torch
+    s = _shape(sB, "sB")
+    if len(s) not in (2, 3):
+        raise ValueError(f"sB must be [ceil(N/128), ceil(K/128)] or [G, ceil(N/128), ceil(K/128)], got {list(s)}")
+    G = s[0] if len(s) == 3 else 1
+    nnb, nkb = -(-N // 128), -(-K // 128)
+    _expect(sB, "sB", s[:-2] + (nnb, nkb))
+    _expect(sB_packed, "sB_packed", s[:-2] + (nnb, -(-nkb // 4)))
+    _check(load().dg_transform_sf_into_ue8m0_b(_ptr(sB, "sB", (torch.float32,)),
+                                               _ptr(sB_packed, "sB_packed", (torch.int32,)), G, N, K, _stream(stream)))
 
 
 def dg_fp8_gemm_nt_ue8m0(A, sA, B, sB, D, stream=None):

@@ -18,6 +18,7 @@
 static_assert(dg::kStatusTimeout == DG_DEV_TIMEOUT, "status bit mismatch");
 static_assert(dg::kStatusBadGroup == DG_DEV_BAD_GROUP_INDEX, "status bit mismatch");
 static_assert(dg::kStatusBadMaskedM == DG_DEV_BAD_MASKED_M, "status bit mismatch");
+static_assert(dg::kStatusBadScale == DG_DEV_BAD_SCALE, "status bit mismatch");
 
 // The device status word: one per device context, read and cleared by dg_get_device_status().
 __device__ int g_dg_device_status;
@@ -813,6 +814,33 @@ dg_status dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0_f32(const uint8_t* A, const 
                                                         const int32_t* sB, const int32_t* k_offsets, float* D, int G,
                                                         int M, int N, int K_total, dg_stream_t stream) {
   return run_k_grouped(true, A, sA, B, sB, k_offsets, D, G, M, N, K_total, static_cast<cudaStream_t>(stream), true);
+}
+
+dg_status dg_transform_sf_into_ue8m0_a(const float* sA, int32_t* sA_packed, int G, int M, int K, dg_stream_t stream) {
+  if (!sA || !sA_packed) return fail(DG_ERR_INVALID_ARG, "null pointer");
+  if (G < 1 || M < 1 || K < 1) return fail(DG_ERR_INVALID_ARG, "G, M and K must be positive");
+  if (!aligned(sA, 4) || !aligned(sA_packed, 4)) return fail(DG_ERR_ALIGNMENT, "scale arrays must be 4-byte aligned");
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  const int nkb = ceil_div(K, 128), ldsa = dg_get_tma_aligned_size(M, 4);
+  const cudaError_t e = dg::launch_sf_pack_a(sA, sA_packed, G, nkb, ldsa, st->status, effective_sms(*st),
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DG_OK : fail_cuda(e, "UE8M0 packing (A) launch");
+}
+
+dg_status dg_transform_sf_into_ue8m0_b(const float* sB, int32_t* sB_packed, int G, int N, int K, dg_stream_t stream) {
+  if (!sB || !sB_packed) return fail(DG_ERR_INVALID_ARG, "null pointer");
+  if (G < 1 || N < 1 || K < 1) return fail(DG_ERR_INVALID_ARG, "G, N and K must be positive");
+  if (!aligned(sB, 4) || !aligned(sB_packed, 4)) return fail(DG_ERR_ALIGNMENT, "scale arrays must be 4-byte aligned");
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  const int nkb = ceil_div(K, 128);
+  const long long rows = (long long)G * ceil_div(N, 128);
+  const cudaError_t e = dg::launch_sf_pack_b(sB, sB_packed, rows, nkb, st->status, effective_sms(*st),
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DG_OK : fail_cuda(e, "UE8M0 packing (B) launch");
 }
 
 dg_status dg_fp8_gemm_nn(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int M,

@@ -52,6 +52,7 @@ enum Mode : int { kDense = 0, kContiguous = 1, kMasked = 2, kKGrouped = 3 };
 
 constexpr int kStatusBadGroup = 0x1;
 constexpr int kStatusBadMaskedM = 0x2;
+constexpr int kStatusBadScale = 0x8;   // a scale packed as UE8M0 was not a power of two (dg_sf_transform.cu)
 
 // Kept at 128 bytes: a larger parameter block made ptxas spill the contiguous form's epilogue.
 struct GemmParams {

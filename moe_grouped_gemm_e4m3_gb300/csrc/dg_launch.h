@@ -45,6 +45,12 @@ cudaError_t launch_bs(const LaunchArgs& a, Mode mode);
 cudaError_t launch_bs_swiglu(const LaunchArgs& a);
 // The block-scaled K-grouped form (MN-major A and B).
 cudaError_t launch_bs_kgrouped(const LaunchArgs& a);
+// FP32 scale factors to packed UE8M0 words (dg_sf_transform.cu). A: [G][nkb][ldsa] ->
+// [G][ceil(nkb/4)][ldsa]; B: [rows][nkb] -> [rows][ceil(nkb/4)] (rows = G * nnb).
+cudaError_t launch_sf_pack_a(const float* sf, int32_t* out, int G, int nkb, int ldsa, int* status, int sms,
+                             cudaStream_t stream);
+cudaError_t launch_sf_pack_b(const float* sf, int32_t* out, long long rows, int nkb, int* status, int sms,
+                             cudaStream_t stream);
 // How many clusters of `cluster` CTAs of the dense / contiguous instantiation for (block_n,
 // out_f32) can be resident at once (0 if the query fails).
 int cluster_capacity_dense(int block_n, bool out_f32, int cluster);

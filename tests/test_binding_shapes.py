@@ -186,3 +186,18 @@ def test_k_grouped_shapes():
     _accepted(dg.dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0, pargs)
     _refused(dg.dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0, pargs, 1, i32(KT // 128, a4(MG)))
     _refused(dg.dg_fp8_k_grouped_gemm_tn_contiguous_ue8m0, pargs, 3, i32(cdiv(NG, 128), KT // 128))
+
+
+def test_transform_sf_shapes():
+    nkq = cdiv(NKB, 4)
+    fa = lambda s, p: dg.dg_transform_sf_into_ue8m0_a(s, p, M, K)
+    fb = lambda s, p: dg.dg_transform_sf_into_ue8m0_b(s, p, N, K)
+    for args in ([f32(NKB, a4(M)), i32(nkq, a4(M))], [f32(G, NKB, a4(M)), i32(G, nkq, a4(M))]):
+        _accepted(fa, args)
+        _refused(fa, args, 1, i32(*args[1].shape[:-2], NKB, a4(M)))      # unpacked K extent
+        _refused(fa, args, 0, f32(*args[0].shape[:-2], NKB, M))          # rows not padded to 4
+    for args in ([f32(NNB, NKB), i32(NNB, nkq)], [f32(G, NNB, NKB), i32(G, NNB, nkq)]):
+        _accepted(fb, args)
+        _refused(fb, args, 1, i32(*args[1].shape[:-1], NKB))
+        _refused(fb, args, 0, f32(*args[0].shape[:-2], NNB + 1, NKB))
+    _refused(fa, [f32(NKB), i32(nkq)], 0, f32(NKB))                       # 1-D is not a layout
