@@ -466,7 +466,8 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}", "wall_ms_per_step": round((t1 - t0) * 1e3 / args.steps, 4)},
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": ({k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")} if e2e else None),
+        "e2e": ({k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "host_buffers_pinned")}
+                if e2e else None),
         "clocks": clocks,
         "gpu_launches": len(tensors) * args.steps,
         "launch_floor_us": round(floor_us, 2),
@@ -625,8 +626,9 @@ def measure_e2e(dg, problems, args, stream):
     torch.cuda.synchronize()
     ms = t_start.elapsed_time(t_end) / steps
     flops = sum(2.0 * h["M"] * h["N"] * h["K"] for h in host)
+    pinned = all(h[n].is_pinned() for h in host for n in ("A", "sA", "B", "sB", "D"))
     return {"value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "host_buffers_pinned": pinned}
 
 
 # ---------------------------------------------------------------------------------------------
