@@ -110,3 +110,27 @@ def test_values_that_are_not_powers_of_two(dg):
     dg.dg_transform_sf_into_ue8m0_b(dev(ok), out2, 512, 128)
     assert dg.dg_get_device_status() == 0
     assert np.array_equal(_bytes(out2.cpu().numpy())[:, 0, 0], np.array([127, 126, 0, 254], np.uint8))
+
+
+def test_masked_layouts_pack_and_drive_the_masked_gemm(dg):
+    # 3-D layouts of the masked form: sA [G, nkb, align4(M_max)], sB [G, nnb, nkb]
+    G, M_max, N, K = 4, 96, 384, 896
+    masked_m = np.array([0, 96, 37, 1], np.int32)
+    a = dg_inputs.make_masked_a(G, M_max, K, seed=13, ue8m0=True)
+    b = dg_inputs.make_b(G, N, K, seed=13, ue8m0=True)
+    nkb = -(-K // 128)
+    pa, pb = _pack_a(dg, a.sA, M_max, K), _pack_b(dg, b.sB, N, K)
+    assert dg.dg_get_device_status() == 0
+    assert np.array_equal(oracle.unpack_ue8m0_a(pa, nkb)[..., :M_max], a.sA[..., :M_max])
+    assert np.array_equal(oracle.unpack_ue8m0_b(pb, nkb), b.sB)
+    D32 = f32_sentinel((G, M_max, N))
+    dg.dg_fp8_grouped_masked_ue8m0_f32(dev(a.A), torch.from_numpy(pa).cuda(), dev(b.B), torch.from_numpy(pb).cuda(),
+                                       dev(masked_m), D32)
+    torch.cuda.synchronize()
+    ref, _, bad = oracle.grouped_masked(a.A, a.sA, b.B, b.sB, masked_m)
+    assert bad == 0
+    valid = np.arange(M_max)[None, :] < masked_m[:, None]
+    d = D32.cpu().numpy()
+    assert np.all(np.isnan(d[~valid])), "rows past masked_m were written"
+    err = np.abs(d[valid].astype(np.float64) - ref[valid]).max() / np.abs(ref[valid]).max()
+    assert err <= 2e-3, err
