@@ -412,6 +412,11 @@ int dg_set_pair_b(int on);
    block-scaled MMA cannot apply it exactly. Device pointers, 4-byte aligned, launched on `stream`;
    the output must not overlap the input. */
 dg_status dg_transform_sf_into_ue8m0_a(const float* sA, int32_t* sA_packed, int G, int M, int K, dg_stream_t stream);
+/* A's FP32 scales from the row-major layout a per-token quantiser writes, sA_rows [G][M][ceil(K/128)]
+   (row m's scales contiguous), into the MN-major layout every call takes, sA [G][ceil(K/128)][align4(M)],
+   rows m >= M set to 0: the other conversion of the library's transform_sf_into_required_layout (same
+   section as above). Device pointers, 4-byte aligned, launched on `stream`; no overlap. */
+dg_status dg_transform_sf_a_into_mn_major(const float* sA_rows, float* sA, int G, int M, int K, dg_stream_t stream);
 dg_status dg_transform_sf_into_ue8m0_b(const float* sB, int32_t* sB_packed, int G, int N, int K, dg_stream_t stream);
 
 /* Programmatic dependent launch for every GEMM call. With on != 0, each kernel is launched with

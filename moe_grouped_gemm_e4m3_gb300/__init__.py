@@ -38,7 +38,8 @@ __all__ = [
     "dg_get_tma_aligned_size", "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms",
     "dg_get_num_sms", "dg_get_device_status", "dg_last_error_string", "dg_query_config",
     "dg_set_tail_splits", "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_set_pdl", "dg_get_pdl",
-    "dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b", "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
+    "dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b", "dg_transform_sf_a_into_mn_major",
+    "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_fp8",
@@ -62,7 +63,8 @@ EXPORTED_SYMBOLS = (
     "dg_get_mk_alignment_for_contiguous_layout", "dg_set_num_sms", "dg_get_num_sms", "dg_get_device_status",
     "dg_last_error_string", "dg_query_config", "dg_fp8_gemm_nt_noalloc", "dg_set_tail_splits",
     "dg_set_cluster_split", "dg_set_wait_limit_us", "dg_set_pair_b", "dg_set_pdl", "dg_get_pdl",
-    "dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b", "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
+    "dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b", "dg_transform_sf_a_into_mn_major",
+    "dg_fp8_gemm_nt_ue8m0", "dg_fp8_gemm_nt_ue8m0_f32", "dg_fp8_grouped_contiguous_ue8m0",
     "dg_fp8_grouped_contiguous_ue8m0_f32", "dg_fp8_grouped_masked_ue8m0", "dg_fp8_grouped_masked_ue8m0_f32",
     "dg_query_config_ue8m0", "dg_fp8_gemm_nt_acc_f32", "dg_fp8_gemm_nt_ue8m0_acc_f32",
     "dg_fp8_grouped_masked_swiglu", "dg_fp8_grouped_masked_swiglu_f32", "dg_fp8_grouped_masked_swiglu_fp8",
@@ -123,7 +125,7 @@ def load(build_if_missing: bool = True):
     lib.dg_set_pair_b.restype, lib.dg_set_pair_b.argtypes = i32, [i32]
     lib.dg_set_pdl.restype, lib.dg_set_pdl.argtypes = i32, [i32]
     lib.dg_get_pdl.restype, lib.dg_get_pdl.argtypes = i32, []
-    for name in ("dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b"):
+    for name in ("dg_transform_sf_into_ue8m0_a", "dg_transform_sf_into_ue8m0_b", "dg_transform_sf_a_into_mn_major"):
         f = getattr(lib, name)
         f.restype, f.argtypes = i32, [P, P, i32, i32, i32, P]
     lib.dg_set_wait_limit_us.restype, lib.dg_set_wait_limit_us.argtypes = ctypes.c_longlong, [ctypes.c_longlong]
@@ -533,6 +535,21 @@ def dg_transform_sf_into_ue8m0_a(sA, sA_packed, M, K, stream=None):
     _expect(sA_packed, "sA_packed", s[:-2] + (-(-nkb // 4), ldsa))
     _check(load().dg_transform_sf_into_ue8m0_a(_ptr(sA, "sA", (torch.float32,)),
                                                _ptr(sA_packed, "sA_packed", (torch.int32,)), G, M, K, _stream(stream)))
+
+
+def dg_transform_sf_a_into_mn_major(sA_rows, sA, M, K, stream=None):
+    """A's FP32 scales row-major sA_rows [M, ceil(K/128)] (or [G, M, ceil(K/128)]) -> the MN-major
+    layout of every call, sA [ceil(K/128), align4(M)] (or [G, ...]), padding rows zero, on the GPU."""
+    import torch
+    s = _shape(sA_rows, "sA_rows")
+    if len(s) not in (2, 3):
+        raise ValueError(f"sA_rows must be [M, ceil(K/128)] or [G, M, ceil(K/128)], got {list(s)}")
+    G = s[0] if len(s) == 3 else 1
+    nkb = -(-K // 128)
+    _expect(sA_rows, "sA_rows", s[:-2] + (M, nkb))
+    _expect(sA, "sA", s[:-2] + (nkb, dg_get_tma_aligned_size(M, 4)))
+    _check(load().dg_transform_sf_a_into_mn_major(_ptr(sA_rows, "sA_rows", (torch.float32,)),
+                                                  _ptr(sA, "sA", (torch.float32,)), G, M, K, _stream(stream)))
 
 
 def dg_transform_sf_into_ue8m0_b(sB, sB_packed, N, K, stream=None):

@@ -829,6 +829,19 @@ dg_status dg_transform_sf_into_ue8m0_a(const float* sA, int32_t* sA_packed, int 
   return e == cudaSuccess ? DG_OK : fail_cuda(e, "UE8M0 packing (A) launch");
 }
 
+dg_status dg_transform_sf_a_into_mn_major(const float* sA_rows, float* sA, int G, int M, int K, dg_stream_t stream) {
+  if (!sA_rows || !sA) return fail(DG_ERR_INVALID_ARG, "null pointer");
+  if (G < 1 || M < 1 || K < 1) return fail(DG_ERR_INVALID_ARG, "G, M and K must be positive");
+  if (!aligned(sA_rows, 4) || !aligned(sA, 4)) return fail(DG_ERR_ALIGNMENT, "scale arrays must be 4-byte aligned");
+  if (G > 65535) return fail(DG_ERR_UNSUPPORTED, "more than 65535 groups");
+  DeviceState* st = nullptr;
+  dg_status s = device_state(&st);
+  if (s != DG_OK) return s;
+  const cudaError_t e = dg::launch_sf_a_to_mn_major(sA_rows, sA, G, M, ceil_div(K, 128), dg_get_tma_aligned_size(M, 4),
+                                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DG_OK : fail_cuda(e, "scale transpose launch");
+}
+
 dg_status dg_transform_sf_into_ue8m0_b(const float* sB, int32_t* sB_packed, int G, int N, int K, dg_stream_t stream) {
   if (!sB || !sB_packed) return fail(DG_ERR_INVALID_ARG, "null pointer");
   if (G < 1 || N < 1 || K < 1) return fail(DG_ERR_INVALID_ARG, "G, N and K must be positive");

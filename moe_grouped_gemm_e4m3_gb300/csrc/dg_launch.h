@@ -51,6 +51,8 @@ cudaError_t launch_sf_pack_a(const float* sf, int32_t* out, int G, int nkb, int 
                              cudaStream_t stream);
 cudaError_t launch_sf_pack_b(const float* sf, int32_t* out, long long rows, int nkb, int* status, int sms,
                              cudaStream_t stream);
+// A's scales row-major [G][M][nkb] -> MN-major [G][nkb][ldsa] (rows m >= M zero).
+cudaError_t launch_sf_a_to_mn_major(const float* in, float* out, int G, int M, int nkb, int ldsa, cudaStream_t stream);
 // How many clusters of `cluster` CTAs of the dense / contiguous instantiation for (block_n,
 // out_f32) can be resident at once (0 if the query fails).
 int cluster_capacity_dense(int block_n, bool out_f32, int cluster);

@@ -1,10 +1,13 @@
-// dg_sf_transform.cu — FP32 scale factors to the packed UE8M0 words of the block-scaled calls.
+// dg_sf_transform.cu — scale-factor layout conversions: A's row-major FP32 scales to the MN-major
+// layout, and FP32 power-of-two scales to the packed UE8M0 words of the block-scaled calls.
 //
 // The SM100 kernels of the pages take their scaling factors as UE8M0 codes packed four to an int32,
 // and the library lists a helper that brings scale factors into that required layout ("DeepGEMM:
 // İnce ölçeklendirmeyle temiz ve verimli FP8 GEMM çekirdekleri", tr.news.hada.io/topic?id=19459,
 // § "GEMM arayüzü ve yerleşim kısıtları" and § "Yardımcı fonksiyonlar ve ortam değişkenleri").
-// Here the input is this library's FP32 layouts and the output its packed layouts:
+// Two conversions. A's FP32 scales as a per-token quantiser writes them (row-major [G][M][nkb]) into the
+// MN-major layout every call takes ([G][nkb][ldsa], rows m >= M zero). And this library's FP32 layouts
+// into its packed layouts:
 //   A: [G][nkb][ldsa] FP32 -> [G][ceil(nkb/4)][ldsa] int32 (MN-major; one thread per word, threads
 //      along the row index so that reads and writes are coalesced);
 //   B: [G][nnb][nkb] FP32 -> [G][nnb][ceil(nkb/4)] int32.
@@ -76,6 +79,26 @@ __global__ void sf_pack_b_kernel(const float* __restrict__ sf, int32_t* __restri
   }
 }
 
+// Row-major A scales [G][M][nkb] -> MN-major [G][nkb][ldsa], rows m >= M zero: one 32x32 tile of the
+// (m, kb) plane per block of 32x8 threads, through shared memory so that both sides are coalesced.
+__global__ void sf_a_to_mn_major_kernel(const float* __restrict__ in, float* __restrict__ out, int M, int nkb,
+                                        int ldsa) {
+  __shared__ float tile[32][33];
+  const int g = blockIdx.z;
+  const int m0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+  const float* src = in + (size_t)g * M * nkb;
+  float* dst = out + (size_t)g * nkb * ldsa;
+  for (int r = threadIdx.y; r < 32; r += 8) {   // read rows m0 + r, columns k0 + threadIdx.x
+    const int m = m0 + r, kb = k0 + threadIdx.x;
+    tile[r][threadIdx.x] = (m < M && kb < nkb) ? src[(size_t)m * nkb + kb] : 0.0f;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += 8) {   // write K-block k0 + r, rows m0 + threadIdx.x
+    const int kb = k0 + r, m = m0 + threadIdx.x;
+    if (kb < nkb && m < ldsa) dst[(size_t)kb * ldsa + m] = tile[threadIdx.x][r];
+  }
+}
+
 int grid_for(long long words, int sms) {
   const long long blocks = (words + 255) / 256;
   const long long cap = 4LL * (sms > 0 ? sms : 1);
@@ -89,6 +112,13 @@ cudaError_t launch_sf_pack_a(const float* sf, int32_t* out, int G, int nkb, int 
   const long long words = (long long)G * ((nkb + 3) / 4) * ldsa;
   if (words == 0) return cudaSuccess;
   sf_pack_a_kernel<<<grid_for(words, sms), 256, 0, stream>>>(sf, out, G, nkb, ldsa, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sf_a_to_mn_major(const float* in, float* out, int G, int M, int nkb, int ldsa, cudaStream_t stream) {
+  if ((long long)G * ldsa * nkb == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((ldsa + 31) / 32), (unsigned)((nkb + 31) / 32), (unsigned)G);
+  sf_a_to_mn_major_kernel<<<grid, dim3(32, 8), 0, stream>>>(in, out, M, nkb, ldsa);
   return cudaGetLastError();
 }
 

@@ -201,3 +201,11 @@ def test_transform_sf_shapes():
         _refused(fb, args, 1, i32(*args[1].shape[:-1], NKB))
         _refused(fb, args, 0, f32(*args[0].shape[:-2], NNB + 1, NKB))
     _refused(fa, [f32(NKB), i32(nkq)], 0, f32(NKB))                       # 1-D is not a layout
+
+
+def test_transform_sf_rows_shapes():
+    f = lambda r, s: dg.dg_transform_sf_a_into_mn_major(r, s, M, K)
+    for args in ([f32(M, NKB), f32(NKB, a4(M))], [f32(G, M, NKB), f32(G, NKB, a4(M))]):
+        _accepted(f, args)
+        _refused(f, args, 0, f32(*args[0].shape[:-2], NKB, M))           # already MN-major
+        _refused(f, args, 1, f32(*args[1].shape[:-2], NKB, M))           # output rows not padded

@@ -134,3 +134,31 @@ def test_masked_layouts_pack_and_drive_the_masked_gemm(dg):
     assert np.all(np.isnan(d[~valid])), "rows past masked_m were written"
     err = np.abs(d[valid].astype(np.float64) - ref[valid]).max() / np.abs(ref[valid]).max()
     assert err <= 2e-3, err
+
+
+@pytest.mark.parametrize("G,M,K", [(1, 198, 1152), (1, 4096, 7168), (3, 70, 640), (2, 1, 128)])
+def test_row_major_scales_to_mn_major(dg, G, M, K):
+    # the MN-major layout of the input generator, handed over row-major and converted back on the GPU
+    a = dg_inputs.make_masked_a(G, M, K, seed=G + M, ue8m0=False)   # sA [G, nkb, align4(M)]
+    rows = np.ascontiguousarray(np.swapaxes(a.sA[..., :M], -1, -2))  # [G, M, nkb]
+    out = torch.full(a.sA.shape, float("nan"), dtype=torch.float32, device="cuda")
+    dg.dg_transform_sf_a_into_mn_major(dev(rows), out, M, K)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.array_equal(got[..., :M], a.sA[..., :M])
+    assert np.all(got[..., M:] == 0.0), "padding rows must be zero"
+
+
+def test_row_major_scales_drive_the_gemm(dg):
+    M, N, K = 200, 264, 768
+    a = dg_inputs.make_a(M, K, seed=17)
+    b = dg_inputs.make_b(1, N, K, seed=17)
+    rows = np.ascontiguousarray(a.sA[:, :M].T)                      # [M, nkb]
+    sA = torch.empty(a.sA.shape, dtype=torch.float32, device="cuda")
+    dg.dg_transform_sf_a_into_mn_major(dev(rows), sA, M, K)
+    D32 = f32_sentinel((M, N))
+    dg.dg_fp8_gemm_nt_f32(dev(a.A), sA, dev(b.B[0]), dev(b.sB[0]), D32)
+    torch.cuda.synchronize()
+    ref64, _ = oracle.gemm_nt(a.A, a.sA, b.B[0], b.sB[0], want_bf16=False)
+    err = np.abs(D32.cpu().numpy().astype(np.float64) - ref64).max() / np.abs(ref64).max()
+    assert err <= 2e-3, err
