@@ -441,6 +441,12 @@ __global__ void __launch_bounds__(Roles<BN, EPI_COLS>::kThreads, 1)
   static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocation: power of two");
   constexpr uint32_t kIdesc = make_idesc_e4m3_f32(128, BN);
   static_assert(kChunks % 2 == 0, "TMEM loads go in pairs");
+  // Two MMA issuers take alternate K-blocks, and each waits on its stages' full barriers and its
+  // TMEM buffers' empty barriers by phase parity. With even STAGES and NBUF every stage and buffer
+  // belongs to one issuer, whose consecutive uses are one phase apart. With an odd count both
+  // issuers would share a stage, and one could wait for the use two phases ahead while the barrier
+  // is still one phase behind: the parity test would pass early and the ring would lose step.
+  static_assert(STAGES % 2 == 0 && NBUF % 2 == 0, "stage and TMEM-buffer counts must be even (two issuers)");
   static_assert(!SWIGLU || (BN == 256 && EPI_COLS == 128 && MODE == kMasked), "fused SwiGLU: masked, BN = 256");
 
   extern __shared__ uint8_t smem_raw[];
